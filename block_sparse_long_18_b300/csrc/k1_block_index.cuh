@@ -1,0 +1,131 @@
+// k1_block_index.cuh -- block compression of the proxy keys.
+//
+// ai4snews item "Step 5 Preview bets on depth over width", Interpretation para 2: the
+// indexer keys of adjacent historical positions are compressed into one representation
+// per block of B = 8 tokens.  Reading: the element-wise mean of the block's token proxies;
+// a partly filled block averages the tokens present.
+//
+// Layout: k_proxy [G, ctx_cap, P] bf16 -> k_blk [G, nb_cap, P] bf16.  Each thread owns 8
+// consecutive proxy elements (one 16-byte vector) of one block, so a warp reads whole
+// 512-byte token rows (P = 256) and writes a whole 512-byte block row.  The sum runs in
+// fp32 in token order; full blocks multiply by 1/B (exact, B is a power of two), partial
+// blocks divide in double so that the result is rounded to bf16 only once.
+#pragma once
+#include "ptx.cuh"
+
+namespace sgqa {
+
+struct K1Args {
+  const __nv_bfloat16* k_proxy;
+  __nv_bfloat16* k_blk;
+  int64_t ctx_cap, nb_cap;
+  int64_t tok_end;      // tokens present
+  int64_t blk_begin;    // first block to build
+  int64_t n_blocks;     // blocks to build per group
+  int32_t G, P, B;
+  // optional per-sequence mode (decode): blocks are given by (kv_off + pos) / B
+  const int64_t* seq_tok_end;  // device or nullptr
+};
+
+__global__ void __launch_bounds__(256) k1_block_index(K1Args a) {
+  const int vec_per_row = a.P / 8;
+  const int64_t n_vec = (int64_t)a.G * a.n_blocks * vec_per_row;
+  const float inv_b = 1.0f / (float)a.B;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += (int64_t)gridDim.x * blockDim.x) {
+    const int pv = (int)(v % vec_per_row);
+    const int64_t gb = v / vec_per_row;
+    const int64_t g = gb / a.n_blocks;
+    const int64_t b = a.blk_begin + gb % a.n_blocks;
+    const int64_t first = b * a.B;
+    int64_t n = a.tok_end - first;
+    if (n > a.B) n = a.B;
+    if (n <= 0) continue;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    const uint4* src = reinterpret_cast<const uint4*>(a.k_proxy + ((g * a.ctx_cap + first) * a.P)) + pv;
+    for (int64_t j = 0; j < n; ++j) {
+      uint4 w = __ldg(src + j * vec_per_row);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(h[e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+      }
+    }
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+    if (n == a.B) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) op[e] = pack_bf16(acc[2 * e] * inv_b, acc[2 * e + 1] * inv_b);
+    } else {
+      const double dn = (double)n;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 lo = __double2bfloat16((double)acc[2 * e] / dn);
+        __nv_bfloat16 hi = __double2bfloat16((double)acc[2 * e + 1] / dn);
+        op[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+      }
+    }
+    reinterpret_cast<uint4*>(a.k_blk + (g * a.nb_cap + b) * a.P)[pv] = o;
+  }
+}
+
+// Decode form: for each sequence s rebuild the block holding its newest token.
+struct K1SeqArgs {
+  const __nv_bfloat16* k_proxy;  // [G, total, P]
+  __nv_bfloat16* k_blk;          // [G, total / B, P]
+  int64_t total;
+  int32_t G, P, B, batch;
+  int64_t ctx_len[256];
+  int64_t kv_off[256];
+};
+
+__global__ void __launch_bounds__(256) k1_block_index_seq(const __grid_constant__ K1SeqArgs a) {
+  const int vec_per_row = a.P / 8;
+  const int n_vec = a.G * a.batch * vec_per_row;
+  const float inv_b = 1.0f / (float)a.B;
+  const int64_t nb_total = a.total / a.B;
+  for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += gridDim.x * blockDim.x) {
+    const int pv = v % vec_per_row;
+    const int s = (v / vec_per_row) % a.batch;
+    const int g = v / (vec_per_row * a.batch);
+    const int64_t L = a.ctx_len[s];
+    const int64_t bl = (L - 1) / a.B;              // block of the newest token (sequence-local)
+    const int64_t first = bl * a.B;
+    const int64_t n = L - first;                   // 1 .. B tokens present
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    const uint4* src =
+        reinterpret_cast<const uint4*>(a.k_proxy + (((int64_t)g * a.total + a.kv_off[s] + first) * a.P)) + pv;
+    for (int64_t j = 0; j < n; ++j) {
+      uint4 w = __ldg(src + j * vec_per_row);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float2 f = __bfloat1622float2(h[e]);
+        acc[2 * e] += f.x;
+        acc[2 * e + 1] += f.y;
+      }
+    }
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+    if (n == a.B) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) op[e] = pack_bf16(acc[2 * e] * inv_b, acc[2 * e + 1] * inv_b);
+    } else {
+      const double dn = (double)n;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 lo = __double2bfloat16((double)acc[2 * e] / dn);
+        __nv_bfloat16 hi = __double2bfloat16((double)acc[2 * e + 1] / dn);
+        op[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+      }
+    }
+    reinterpret_cast<uint4*>(a.k_blk + ((int64_t)g * nb_total + a.kv_off[s] / a.B + bl) * a.P)[pv] = o;
+  }
+}
+
+}  // namespace sgqa

@@ -1,0 +1,91 @@
+// k2d_decode_index.cuh -- indexer scores for decode: one query proxy per (sequence, group)
+// against that sequence's earlier block proxies.  Same definition as the prefill indexer
+// (a plain dot product, fp32 accumulation; ai4snews item, Interpretation para 2), but with
+// a single query row it is a matrix-vector product that streams the block-proxy cache
+// from HBM: one warp reads one 512-byte block row per load (P = 256), four rows in flight.
+#pragma once
+#include "ptx.cuh"
+
+namespace sgqa {
+
+struct K2dArgs {
+  const __nv_bfloat16* qp;    // [G, batch, P]
+  const __nv_bfloat16* kblk;  // [G, nb_total, P]
+  float* scores;              // [G, batch, ld]
+  int64_t ld, nb_total;
+  int32_t G, P, B, batch;
+  int32_t rows_per_cta;
+  int64_t ctx_len[256];
+  int64_t kv_off[256];
+};
+
+__global__ void __launch_bounds__(256) k2d_decode_index(const __grid_constant__ K2dArgs a) {
+  const int gs = blockIdx.y;  // g * batch + s
+  const int g = gs / a.batch, s = gs % a.batch;
+  const int64_t n = (a.ctx_len[s] - 1) / a.B;  // candidates 0 .. b_t - 1
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = a.P / 8;
+  const bool active = lane < nvec;
+  float qv[8];
+  {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (active) w = __ldg(reinterpret_cast<const uint4*>(a.qp + ((int64_t)g * a.batch + s) * a.P) + lane);
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(h[e]);
+      qv[2 * e] = f.x;
+      qv[2 * e + 1] = f.y;
+    }
+  }
+  const __nv_bfloat16* base = a.kblk + ((int64_t)g * a.nb_total + a.kv_off[s] / a.B) * a.P;
+  float* out = a.scores + (int64_t)gs * a.ld;
+  const int64_t b_lo = (int64_t)blockIdx.x * a.rows_per_cta;
+  int64_t b_hi = b_lo + a.rows_per_cta;
+  if (b_hi > n) b_hi = n;
+  for (int64_t b0 = b_lo + warp * 4; b0 < b_hi; b0 += 8 * 4) {
+    float acc[4];
+    uint4 w[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      w[r] = make_uint4(0, 0, 0, 0);
+      if (active && b0 + r < b_hi) w[r] = __ldg(reinterpret_cast<const uint4*>(base + (b0 + r) * a.P) + lane);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[r]);
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        sum = fmaf(qv[2 * e], f.x, sum);
+        sum = fmaf(qv[2 * e + 1], f.y, sum);
+      }
+      acc[r] = sum;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+        if (b0 + r < b_hi) out[b0 + r] = acc[r];
+    }
+  }
+}
+
+// Bounded-wait self test: waits on an mbarrier that nothing ever arrives at.  The wait
+// gives up after limit_ns and records the timeout in the device error word.
+__global__ void k_selftest_wait(uint64_t limit_ns, int32_t* result) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    const bool ok = mbar_wait(smem_u32(&bar), 0, limit_ns);
+    if (result) *result = ok ? 1 : 0;
+  }
+}
+
+}  // namespace sgqa

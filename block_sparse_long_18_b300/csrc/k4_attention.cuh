@@ -1,0 +1,425 @@
+// k4_attention.cuh -- gated sparse attention over the selected blocks.
+//
+// ai.info article "StepFun Details Step 5 Preview's 92-Block Agent Design", "Why StepFun
+// chose 92 transformer blocks": the full-attention path is Gated GQA; ai4snews item,
+// Interpretation para 2: a sparse flash-attention operator runs over the selected blocks;
+// phantomic12 entry: 64 heads in 4 KV groups, head_dim 192.
+//
+//   for row i (position t), group g, head h in g:  J = { j in selected blocks : j <= t }
+//   o = softmax_j(scale * q_h . k_j) . v_j ;  out = o * sigmoid(gate) ;  lse = log sum exp
+//
+// One warp owns one (row, group) unit: its 16 heads are the M = 16 of mma.sync m16n8k16
+// (bf16 in, fp32 accumulate), so every gathered K/V byte serves all 16 heads.  The warp
+// walks its selection 16 keys per stage (two blocks of 8).  Each block of a group is one
+// contiguous 8 x 192 bf16 run in the group-major cache, fetched by ONE TMA copy per
+// tensor through a 3-D tensor map {64, 3, tokens} with 128-byte swizzle; the smem row of
+// (token n, 64-wide chunk c) is 3n + c, and since 3 is odd, ldmatrix over 8 consecutive
+// tokens of one chunk touches 8 distinct 16-byte bank groups.  Stages cycle through a
+// per-warp ring of mbarriers (bounded waits).  S = Q K^T (2 n-tiles x 12 k-steps), online
+// softmax in fp32 (exp2 domain, masked keys -inf), P goes straight from the accumulator
+// layout into the A operand of P V (24 n-tiles over D).  The epilogue normalises, applies
+// sigmoid(gate) and writes bf16 through a swizzled smem tile with 16-byte stores.
+//
+// Units are numbered group-major, so the CTAs in flight at any moment gather from one
+// group's K/V (100 MB at 128K tokens), which the 126 MB L2 can hold.
+//
+// Split-K (decode): unit = (row, group, split); a split walks a range of stages and
+// writes fp32 partials (m, l, O) that k4_combine merges with LSE weights.
+#pragma once
+#include "ptx.cuh"
+
+namespace sgqa {
+
+constexpr int K4_D = 192;
+constexpr int K4_UNITS = K4_D / 8;            // 16-byte units per row: 24
+constexpr uint32_t K4_TILE = 16 * K4_D * 2;   // 16 keys x 192 bf16 = 6144 B
+constexpr uint32_t K4_STAGE = 2 * K4_TILE;    // K + V
+
+struct K4Args {
+  const __nv_bfloat16* q;       // [rows, H, D]
+  const __nv_bfloat16* gate;    // [rows, H, D] or [rows, H]
+  const __nv_bfloat16* kc;      // [G, ctx_cap, D]  (cp.async loader)
+  const __nv_bfloat16* vc;
+  __nv_bfloat16* out;           // [rows, H, D]
+  float* lse;                   // [rows, H] or null
+  const int32_t* sel_idx;       // [G, rows, kcap]
+  const int32_t* sel_cnt;       // [G, rows]
+  float* part_o;                // split mode: [units, 16, D]
+  float* part_ml;               // split mode: [units, 16, 2]
+  int64_t rows;
+  int64_t pos0;
+  int64_t ctx_cap;
+  int32_t G, Hg, H, B, kcap;
+  float scale_log2;
+  int32_t dense;
+  int32_t gate_per_dim;
+  int32_t nsplit;
+  int32_t use_pos;
+  uint64_t wait_ns;
+  int64_t pos[256];
+  int64_t kv_off[256];
+};
+
+// byte offset, inside a 16-key tile, of 16-byte unit u (0..23) of key n (0..15)
+__device__ __forceinline__ uint32_t k4_off(uint32_t n, uint32_t u) {
+  const uint32_t r = n * 3 + (u >> 3);
+  return r * 128 + (((u & 7) ^ (r & 7)) << 4);
+}
+
+template <int NW, int NSTAGE, bool TMA>
+__global__ void __launch_bounds__(NW * 32, 1)
+    k4_sparse_attn(const __grid_constant__ K4Args a, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t k4_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(k4_smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const uint32_t wbase = smem_u32(smem) + warp * (NSTAGE * K4_STAGE);
+  const uint32_t bar0 = smem_u32(smem) + NW * NSTAGE * K4_STAGE + warp * NSTAGE * 8;
+
+  const int64_t n_units = (int64_t)a.G * a.rows * a.nsplit;
+  const int64_t unit = (int64_t)blockIdx.x * NW + warp;
+  if (unit >= n_units) return;
+  const int32_t split = (int32_t)(unit % a.nsplit);
+  const int64_t gr = unit / a.nsplit;
+  const int32_t g = (int32_t)(gr / a.rows);
+  const int64_t i = gr % a.rows;
+  const int64_t t = a.use_pos ? a.pos[i] : a.pos0 + i;
+  const int64_t kvo = a.use_pos ? a.kv_off[i] : 0;
+  const int64_t bt = t / a.B;
+  const int32_t* sel = a.sel_idx + (g * a.rows + i) * (int64_t)a.kcap;
+  int64_t cnt = a.dense ? bt + 1 : (int64_t)a.sel_cnt[g * a.rows + i];
+  if (cnt < 1 || cnt > (a.dense ? bt + 1 : (int64_t)a.kcap)) {
+    report_error(kErrBounds);
+    cnt = cnt < 1 ? 1 : (a.dense ? bt + 1 : a.kcap);
+  }
+  const int bps = 16 / a.B;  // blocks per stage
+  const int64_t n_st = (cnt + bps - 1) / bps;
+  const int64_t per_split = (n_st + a.nsplit - 1) / a.nsplit;
+  const int64_t s_begin = (int64_t)split * per_split;
+  const int64_t s_end = s_begin + per_split < n_st ? s_begin + per_split : n_st;
+
+  auto block_of = [&](int64_t j) -> int64_t {  // j-th selected block, or -1 if unused/invalid
+    if (j >= cnt) return -1;
+    const int64_t b = a.dense ? j : (int64_t)__ldg(sel + j);
+    return (b >= 0 && b <= bt) ? b : -2;
+  };
+
+  // ---- Q fragments: Q[i, g*Hg + h, :] staged swizzled in slot 0, then ldmatrix ----
+  const uint32_t qs = wbase;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.q + (i * a.H + (int64_t)g * a.Hg) * K4_D);
+    for (int w = lane; w < 16 * K4_UNITS; w += 32) {
+      const uint32_t h = w / K4_UNITS, u = w % K4_UNITS;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if ((int)h < a.Hg) v = __ldg(src + w);
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + k4_off(h, u)), "r"(v.x), "r"(v.y), "r"(v.z),
+                   "r"(v.w)
+                   : "memory");
+    }
+  }
+  __syncwarp();
+  uint32_t qa[12][4];
+#pragma unroll
+  for (int ks = 0; ks < 12; ++ks) {
+    // matrices: (heads 0-7, unit 2ks), (heads 8-15, unit 2ks), (0-7, 2ks+1), (8-15, 2ks+1)
+    const uint32_t m = lane >> 3;
+    const uint32_t h = (m & 1) * 8 + (lane & 7);
+    const uint32_t u = 2 * ks + (m >> 1);
+    ldsm_x4(qs + k4_off(h, u), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+  }
+  __syncwarp();
+
+  if (TMA && lane == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+
+  // ---- stage loader ----
+  auto issue = [&](int64_t s) {
+    const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
+    const uint32_t ks_addr = wbase + slot * K4_STAGE;
+    const uint32_t vs_addr = ks_addr + K4_TILE;
+    if (TMA) {
+      if (lane == 0) {
+        const uint32_t bar = bar0 + 8 * slot;
+        mbar_arrive_expect_tx(bar, K4_STAGE);
+        for (int bi = 0; bi < bps; ++bi) {
+          int64_t b = block_of(s * bps + bi);
+          if (b < 0) b = bt;  // unused / invalid slot: fetch the own block, masked below
+          const int32_t row = (int32_t)((int64_t)g * a.ctx_cap + kvo + b * a.B);
+          tma_load_3d(ks_addr + bi * a.B * 384, &tmK, bar, 0, 0, row);
+          tma_load_3d(vs_addr + bi * a.B * 384, &tmV, bar, 0, 0, row);
+        }
+      }
+    } else {
+      const int64_t row_lim = (int64_t)a.G * a.ctx_cap - 1;
+      for (int w = lane; w < 16 * K4_UNITS; w += 32) {
+        const uint32_t n = w / K4_UNITS, u = w % K4_UNITS;
+        int64_t b = block_of(s * bps + n / a.B);
+        if (b < 0) b = bt;
+        int64_t row = (int64_t)g * a.ctx_cap + kvo + b * a.B + (n % a.B);
+        if (row > row_lim) row = row_lim;
+        const uint32_t off = k4_off(n, u);
+        cp_async_16(ks_addr + off, a.kc + row * K4_D + u * 8);
+        cp_async_16(vs_addr + off, a.vc + row * K4_D + u * 8);
+      }
+      cp_async_commit();
+    }
+  };
+
+  float o[24][4];
+#pragma unroll
+  for (int d = 0; d < 24; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const uint32_t qd = lane & 3;  // column pair within an 8-wide tile
+  bool ok = true;
+  int64_t issued = s_begin;
+
+  for (int s = 0; s < NSTAGE - 1; ++s)
+    if (s_begin + s < s_end) { issue(s_begin + s); issued = s_begin + s + 1; }
+    else if (!TMA) cp_async_commit();
+
+  for (int64_t s = s_begin; s < s_end; ++s) {
+    if (s + NSTAGE - 1 < s_end) { issue(s + NSTAGE - 1); issued = s + NSTAGE; }
+    else if (!TMA) cp_async_commit();
+    const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
+    if (TMA) {
+      if (!mbar_wait(bar0 + 8 * slot, (uint32_t)(((s - s_begin) / NSTAGE) & 1), a.wait_ns)) { ok = false; break; }
+    } else {
+      cp_async_wait<NSTAGE - 1>();
+      __syncwarp();
+    }
+    const uint32_t ks_addr = wbase + slot * K4_STAGE;
+    const uint32_t vs_addr = ks_addr + K4_TILE;
+
+    // ---- S = Q K^T ----
+    float sc[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+    for (int kp = 0; kp < 12; kp += 2) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(ks_addr + k4_off(nt * 8 + (lane & 7), 2 * kp + (lane >> 3)), b0, b1, b2, b3);
+        mma_bf16_16816(sc[nt], qa[kp], b0, b1);
+        mma_bf16_16816(sc[nt], qa[kp + 1], b2, b3);
+      }
+    }
+
+    // ---- mask: unused slots, invalid indices, and tokens after t in the own block ----
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const int key = nt * 8 + 2 * qd + c;
+        const int64_t b = block_of(s * bps + key / a.B);
+        const bool valid = b >= 0 && b * a.B + (key % a.B) <= t;
+        if (b == -2 && c == 0 && nt == 0 && lane == 0) report_error(kErrBounds);
+        sc[nt][c] = valid ? sc[nt][c] * a.scale_log2 : -INFINITY;
+        sc[nt][2 + c] = valid ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+      }
+    }
+
+    // ---- online softmax (rows r = lane/4 and r + 8) ----
+    float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+    float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
+    const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
+    m0 = mn0;
+    m1 = mn1;
+    float p[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      p[nt][0] = fast_exp2(sc[nt][0] - mu0);
+      p[nt][1] = fast_exp2(sc[nt][1] - mu0);
+      p[nt][2] = fast_exp2(sc[nt][2] - mu1);
+      p[nt][3] = fast_exp2(sc[nt][3] - mu1);
+    }
+    l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
+    l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
+#pragma unroll
+    for (int d = 0; d < 24; ++d) {
+      o[d][0] *= al0;
+      o[d][1] *= al0;
+      o[d][2] *= al1;
+      o[d][3] *= al1;
+    }
+    uint32_t pa[4];
+    pa[0] = pack_bf16(p[0][0], p[0][1]);
+    pa[1] = pack_bf16(p[0][2], p[0][3]);
+    pa[2] = pack_bf16(p[1][0], p[1][1]);
+    pa[3] = pack_bf16(p[1][2], p[1][3]);
+
+    // ---- O += P V ----
+#pragma unroll
+    for (int dp = 0; dp < 12; ++dp) {
+      const uint32_t mtx = lane >> 3;
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vs_addr + k4_off((mtx & 1) * 8 + (lane & 7), 2 * dp + (mtx >> 1)), v0, v1, v2, v3);
+      mma_bf16_16816(o[2 * dp], pa, v0, v1);
+      mma_bf16_16816(o[2 * dp + 1], pa, v2, v3);
+    }
+    __syncwarp();
+  }
+
+  if (!ok) {
+    // drain the copies still in flight into this warp's slots, then leave
+    if (TMA && lane == 0) {
+      for (int64_t s = issued - NSTAGE > s_begin ? issued - NSTAGE : s_begin; s < issued; ++s) {
+        const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
+        mbar_wait(bar0 + 8 * slot, (uint32_t)(((s - s_begin) / NSTAGE) & 1), kDrainLimitNs);
+      }
+    }
+    __syncwarp();
+    return;
+  }
+  if (!TMA) cp_async_wait<0>();
+  __syncwarp();
+
+  // full row sums across the quad
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  const uint32_t r0 = lane >> 2, r1 = r0 + 8;
+
+  if (a.nsplit > 1) {
+    float* po = a.part_o + unit * (16 * K4_D);
+    float* pml = a.part_ml + unit * 32;
+#pragma unroll
+    for (int d = 0; d < 24; ++d) {
+      const int col = d * 8 + 2 * qd;
+      *reinterpret_cast<float2*>(po + r0 * K4_D + col) = make_float2(o[d][0], o[d][1]);
+      *reinterpret_cast<float2*>(po + r1 * K4_D + col) = make_float2(o[d][2], o[d][3]);
+    }
+    if (qd == 0) {
+      pml[r0 * 2] = m0;
+      pml[r0 * 2 + 1] = l0;
+      pml[r1 * 2] = m1;
+      pml[r1 * 2 + 1] = l1;
+    }
+    return;
+  }
+
+  // ---- epilogue: normalise, gate, bf16, coalesced store ----
+  const float inv0 = l0 > 0.f ? __frcp_rn(l0) : 0.f;
+  const float inv1 = l1 > 0.f ? __frcp_rn(l1) : 0.f;
+  const uint32_t ts = wbase;  // slot 0 is free: every issued stage has been consumed
+  const int64_t head0 = i * a.H + (int64_t)g * a.Hg;
+  if (a.gate_per_dim) {
+    const uint4* src = reinterpret_cast<const uint4*>(a.gate + head0 * K4_D);
+    for (int w = lane; w < a.Hg * K4_UNITS; w += 32) {
+      const uint4 v = __ldg(src + w);
+      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(ts + k4_off(w / K4_UNITS, w % K4_UNITS)),
+                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+    }
+  }
+  __syncwarp();
+  const float kLog2e = 1.4426950408889634f;
+  float gh0 = 0.f, gh1 = 0.f;
+  if (!a.gate_per_dim) {
+    if ((int)r0 < a.Hg) gh0 = __bfloat162float(a.gate[head0 + r0]);
+    if ((int)r1 < a.Hg) gh1 = __bfloat162float(a.gate[head0 + r1]);
+  }
+#pragma unroll
+  for (int d = 0; d < 24; ++d) {
+    const uint32_t col = d * 8 + 2 * qd;
+    const uint32_t a0 = ts + k4_off(r0, col >> 3) + (col & 7) * 2;
+    const uint32_t a1 = ts + k4_off(r1, col >> 3) + (col & 7) * 2;
+    float g00 = gh0, g01 = gh0, g10 = gh1, g11 = gh1;
+    if (a.gate_per_dim) {
+      uint32_t w0, w1;
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w0) : "r"(a0));
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w1) : "r"(a1));
+      const float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w0));
+      const float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w1));
+      g00 = f0.x; g01 = f0.y; g10 = f1.x; g11 = f1.y;
+    }
+    const float s00 = __frcp_rn(1.f + fast_exp2(-g00 * kLog2e));
+    const float s01 = __frcp_rn(1.f + fast_exp2(-g01 * kLog2e));
+    const float s10 = __frcp_rn(1.f + fast_exp2(-g10 * kLog2e));
+    const float s11 = __frcp_rn(1.f + fast_exp2(-g11 * kLog2e));
+    const uint32_t w0 = pack_bf16(o[d][0] * inv0 * s00, o[d][1] * inv0 * s01);
+    const uint32_t w1 = pack_bf16(o[d][2] * inv1 * s10, o[d][3] * inv1 * s11);
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a0), "r"(w0) : "memory");
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(a1), "r"(w1) : "memory");
+  }
+  __syncwarp();
+  {
+    uint4* dst = reinterpret_cast<uint4*>(a.out + head0 * K4_D);
+    for (int w = lane; w < a.Hg * K4_UNITS; w += 32) {
+      uint4 v;
+      asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                   : "r"(ts + k4_off(w / K4_UNITS, w % K4_UNITS)));
+      dst[w] = v;
+    }
+  }
+  if (a.lse && qd == 0) {
+    const float kLn2 = 0.6931471805599453f;
+    if ((int)r0 < a.Hg) a.lse[head0 + r0] = (m0 + __log2f(l0)) * kLn2;
+    if ((int)r1 < a.Hg) a.lse[head0 + r1] = (m1 + __log2f(l1)) * kLn2;
+  }
+}
+
+// Merge split-K partials: one warp per (row, group, head).
+struct K4CombineArgs {
+  const float* part_o;     // [G*rows*nsplit, 16, D]
+  const float* part_ml;    // [G*rows*nsplit, 16, 2]
+  const __nv_bfloat16* gate;
+  __nv_bfloat16* out;
+  float* lse;
+  int64_t rows;
+  int32_t G, Hg, H, nsplit, gate_per_dim;
+};
+
+__global__ void __launch_bounds__(256) k4_combine(const K4CombineArgs a) {
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const uint32_t lane = lane_id();
+  const int64_t total = (int64_t)a.G * a.rows * a.Hg;
+  if (wid >= total) return;
+  const int h = (int)(wid % a.Hg);
+  const int64_t gr = wid / a.Hg;           // = g * rows + i
+  const int g = (int)(gr / a.rows);
+  const int64_t i = gr % a.rows;
+  float M = -INFINITY;
+  for (int s = 0; s < a.nsplit; ++s) {
+    const float* ml = a.part_ml + ((gr * a.nsplit + s) * 16 + h) * 2;
+    if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+  }
+  float L = 0.f;
+  float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < a.nsplit; ++s) {
+    const int64_t u = gr * a.nsplit + s;
+    const float* ml = a.part_ml + (u * 16 + h) * 2;
+    if (!(ml[1] > 0.f)) continue;
+    const float w = fast_exp2(ml[0] - M);
+    L += w * ml[1];
+    const float* po = a.part_o + (u * 16 + h) * K4_D;
+#pragma unroll
+    for (int e = 0; e < 6; ++e) acc[e] += w * po[lane + 32 * e];
+  }
+  const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
+  const int64_t head = i * a.H + (int64_t)g * a.Hg + h;
+  const float kLog2e = 1.4426950408889634f;
+#pragma unroll
+  for (int e = 0; e < 6; ++e) {
+    const int d = lane + 32 * e;
+    const float gv = a.gate_per_dim ? __bfloat162float(a.gate[head * K4_D + d]) : __bfloat162float(a.gate[head]);
+    const float sg = __frcp_rn(1.f + fast_exp2(-gv * kLog2e));
+    a.out[head * K4_D + d] = __float2bfloat16_rn(acc[e] * inv * sg);
+  }
+  if (a.lse && lane == 0) a.lse[head] = (M + __log2f(L)) * 0.6931471805599453f;
+}
+
+}  // namespace sgqa

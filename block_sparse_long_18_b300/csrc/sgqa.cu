@@ -1,0 +1,599 @@
+// sgqa.cu -- the C ABI of the Sparse GQA layer (include/sgqa.h): argument checks,
+// workspace carving, TMA tensor maps and the launch sequence of the four stages
+// (block index -> indexer -> top-k -> gated sparse attention) and of decode.
+//
+// Single translation unit: the kernels live in the .cuh files included below.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sgqa.h"
+#include "ptx.cuh"
+#include "k1_block_index.cuh"
+#include "k2_indexer.cuh"
+#include "k2d_decode_index.cuh"
+#include "k3_topk.cuh"
+#include "k4_attention.cuh"
+
+using namespace sgqa;
+
+namespace {
+
+uint64_t g_wait_ns = 1000000000ull;
+
+constexpr int64_t kIndexChunkRows = 8192;  // preferred query rows per indexer/top-k pass
+constexpr int kMaxBatch = 256;
+constexpr int kK3Threads = 512;
+constexpr int kK3Per = 32;
+constexpr int64_t kK3RegRow = (int64_t)kK3Threads * kK3Per;  // rows up to this many candidates stay in registers
+
+#define SGQA_CUDA_OK(expr)                       \
+  do {                                           \
+    if ((expr) != cudaSuccess) return SGQA_ERR_CUDA; \
+  } while (0)
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Parameters after defaults are resolved.
+struct Prm {
+  int G, Hg, H, D, P, B, k, gate_per_dim;
+  float scale;
+};
+
+sgqa_status check_params(const sgqa_params* p, Prm& o) {
+  if (!p) return SGQA_ERR_INVALID_ARGUMENT;
+  if (p->num_kv_groups < 1 || p->heads_per_group < 1 || p->head_dim < 1 || p->proxy_dim < 1 || p->block_size < 1 ||
+      p->top_k_blocks < 1)
+    return SGQA_ERR_INVALID_ARGUMENT;
+  if (p->heads_per_group > 16 || p->head_dim != 192) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (p->proxy_dim % 64 != 0 || p->proxy_dim > 256) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  const int B = p->block_size;
+  if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (p->gate_per_dim != 0 && p->gate_per_dim != 1) return SGQA_ERR_INVALID_ARGUMENT;
+  o.G = p->num_kv_groups;
+  o.Hg = p->heads_per_group;
+  o.H = o.G * o.Hg;
+  o.D = p->head_dim;
+  o.P = p->proxy_dim;
+  o.B = B;
+  o.k = p->top_k_blocks;
+  o.gate_per_dim = p->gate_per_dim;
+  o.scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)o.D);
+  return SGQA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D tiled tensor map with 128-byte swizzle.  dims/box innermost first; strides in bytes
+// for dims 1 and 2.
+bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint64_t s1, uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {s1, s2};
+  const cuuint32_t box[3] = {b0, b1, b2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 148;
+  }
+  return n;
+}
+
+// ---- attention launch configuration (warps per CTA, stages per warp) ----
+struct K4Cfg {
+  int nw, ns;
+};
+K4Cfg k4_cfg() {
+  static K4Cfg c = [] {
+    K4Cfg d{4, 4};
+    if (const char* e = std::getenv("SGQA_K4_CFG")) {
+      int a = 0, b = 0;
+      if (std::sscanf(e, "%dx%d", &a, &b) == 2) {
+        if ((a == 4 && b == 4) || (a == 8 && b == 2) || (a == 6 && b == 3) || (a == 4 && b == 3) || (a == 8 && b == 3))
+          d = K4Cfg{a, b};
+      }
+    }
+    return d;
+  }();
+  return c;
+}
+
+size_t k4_smem(int nw, int ns) { return (size_t)nw * ns * K4_STAGE + (size_t)nw * ns * 8 + 1024; }
+
+template <int NW, int NS, bool TMA>
+cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
+                        cudaStream_t st) {
+  const size_t smem = k4_smem(NW, NS);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k4_sparse_attn<NW, NS, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t grid = cdiv(n_units, NW);
+  k4_sparse_attn<NW, NS, TMA><<<(unsigned)grid, NW * 32, smem, st>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_k4(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units, bool tma,
+                      cudaStream_t st) {
+  if (!tma) return launch_k4_t<4, 4, false>(a, tk, tv, n_units, st);
+  const K4Cfg c = k4_cfg();
+  if (c.nw == 8 && c.ns == 2) return launch_k4_t<8, 2, true>(a, tk, tv, n_units, st);
+  if (c.nw == 6 && c.ns == 3) return launch_k4_t<6, 3, true>(a, tk, tv, n_units, st);
+  if (c.nw == 4 && c.ns == 3) return launch_k4_t<4, 3, true>(a, tk, tv, n_units, st);
+  if (c.nw == 8 && c.ns == 3) return launch_k4_t<8, 3, true>(a, tk, tv, n_units, st);
+  return launch_k4_t<4, 4, true>(a, tk, tv, n_units, st);
+}
+
+cudaError_t launch_k2(const K2Args& a, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
+                      cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(k2_indexer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t grid = std::min<int64_t>(a.n_items, num_sms());
+  if (grid <= 0) return cudaSuccess;
+  k2_indexer<<<(unsigned)grid, K2_THREADS, K2_SMEM_BYTES, st>>>(a, ta, tb, tc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_k3(const K3Args& a, int64_t max_cand, cudaStream_t st) {
+  const int64_t grid = (int64_t)a.G * a.rows;
+  if (grid <= 0) return cudaSuccess;
+  if (max_cand <= kK3RegRow)
+    k3_topk<kK3Threads, kK3Per, false><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
+  else
+    k3_topk<kK3Threads, kK3Per, true><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_k1(const K1Args& a, cudaStream_t st) {
+  const int64_t n_vec = (int64_t)a.G * a.n_blocks * (a.P / 8);
+  if (n_vec <= 0) return cudaSuccess;
+  const int64_t grid = std::min<int64_t>(cdiv(n_vec, 256), (int64_t)num_sms() * 16);
+  k1_block_index<<<(unsigned)grid, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// Bytes of the indexer score workspace for `rows` query rows whose largest candidate count
+// is max_cand.
+size_t index_ws_bytes(const Prm& p, int64_t rows, int64_t max_cand) {
+  const int64_t ld = std::max<int64_t>(4, align_up((size_t)max_cand, 4));
+  return align_up((size_t)p.G * rows * ld * 4, 256);
+}
+
+// ---- the indexer + top-k over rows [0, T) at positions q_start .. ----
+sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t q_start, const void* k_blk,
+                           int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes,
+                           cudaStream_t st) {
+  const int64_t max_cand = (q_start + T - 1) / p.B;  // candidates of the last row
+  const int64_t ld = std::max<int64_t>(4, (int64_t)align_up((size_t)max_cand, 4));
+  // rows per pass: as many as the workspace holds, preferring kIndexChunkRows
+  int64_t rows = std::min<int64_t>(T, kIndexChunkRows);
+  const size_t per_row = (size_t)p.G * ld * 4;
+  const int64_t fit = (int64_t)(ws_bytes / per_row);
+  if (fit < rows) {
+    rows = fit >= 128 ? fit / 128 * 128 : fit;
+    if (rows < std::min<int64_t>(T, 128)) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  }
+  if (!aligned16(ws)) return SGQA_ERR_INVALID_ARGUMENT;
+  float* scores = static_cast<float*>(ws);
+
+  CUtensorMap ta, tb;
+  if (!make_map_3d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q_proxy, p.P, T, p.G, (uint64_t)p.P * 2,
+                   (uint64_t)T * p.P * 2, 64, 128, 1))
+    return SGQA_ERR_CUDA;
+  if (!make_map_3d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_blk, p.P, nb_cap, p.G, (uint64_t)p.P * 2,
+                   (uint64_t)nb_cap * p.P * 2, 64, 128, 1))
+    return SGQA_ERR_CUDA;
+
+  for (int64_t r0 = 0; r0 < T; r0 += rows) {
+    const int64_t rc = std::min<int64_t>(rows, T - r0);
+    const int64_t cand_last = (q_start + r0 + rc - 1) / p.B;
+    if (cand_last > 0) {
+      CUtensorMap tc;
+      if (!make_map_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scores, ld, rc, p.G, (uint64_t)ld * 4,
+                       (uint64_t)rc * ld * 4, 32, 32, 1))
+        return SGQA_ERR_CUDA;
+      K2Args a2{};
+      a2.G = p.G;
+      a2.P = p.P;
+      a2.B = p.B;
+      a2.kch = p.P / 64;
+      a2.Tc = rc;
+      a2.row_base = r0;
+      a2.pos0 = q_start + r0;
+      a2.n_mtiles = (int32_t)cdiv(rc, 128);
+      a2.nti = 8;
+      a2.items_per_m = (int32_t)cdiv(cdiv(cand_last, 128), a2.nti);
+      a2.n_items = (int64_t)p.G * a2.n_mtiles * a2.items_per_m;
+      a2.ld = ld;
+      a2.wait_ns = g_wait_ns;
+      SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
+    }
+    K3Args a3{};
+    a3.scores = scores;
+    a3.ld = ld;
+    a3.rows = rc;
+    a3.pos0 = q_start + r0;
+    a3.out_row0 = r0;
+    a3.T_out = T;
+    a3.G = p.G;
+    a3.B = p.B;
+    a3.k = p.k;
+    a3.sel_idx = sel_idx;
+    a3.sel_cnt = sel_cnt;
+    a3.use_pos = 0;
+    SGQA_CUDA_OK(launch_k3(a3, cand_last, st));
+  }
+  return SGQA_OK;
+}
+
+sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void* v, int64_t ctx_cap, const void* gate,
+                          const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T, int64_t q_start, void* out,
+                          float* lse, int32_t dense, cudaStream_t st) {
+  K4Args a{};
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.gate = static_cast<const __nv_bfloat16*>(gate);
+  a.kc = static_cast<const __nv_bfloat16*>(k);
+  a.vc = static_cast<const __nv_bfloat16*>(v);
+  a.out = static_cast<__nv_bfloat16*>(out);
+  a.lse = lse;
+  a.sel_idx = sel_idx;
+  a.sel_cnt = sel_cnt;
+  a.rows = T;
+  a.pos0 = q_start;
+  a.ctx_cap = ctx_cap;
+  a.G = p.G;
+  a.Hg = p.Hg;
+  a.H = p.H;
+  a.B = p.B;
+  a.kcap = p.k;
+  a.scale_log2 = p.scale * 1.4426950408889634f;
+  a.dense = dense;
+  a.gate_per_dim = p.gate_per_dim;
+  a.nsplit = 1;
+  a.use_pos = 0;
+  a.wait_ns = g_wait_ns;
+  const bool tma = p.B >= 8;
+  CUtensorMap tk{}, tv{};
+  if (tma) {
+    const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
+    if (!make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, 64, 3, rowsz, 128, 384, 64, 3, p.B)) return SGQA_ERR_CUDA;
+    if (!make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, 64, 3, rowsz, 128, 384, 64, 3, p.B)) return SGQA_ERR_CUDA;
+  }
+  SGQA_CUDA_OK(launch_k4(a, tk, tv, (int64_t)p.G * T, tma, st));
+  return SGQA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sgqa_status_string(sgqa_status s) {
+  switch (s) {
+    case SGQA_OK: return "ok";
+    case SGQA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case SGQA_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case SGQA_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case SGQA_ERR_CUDA: return "CUDA runtime error";
+    case SGQA_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case SGQA_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+  }
+  return "unknown status";
+}
+
+int32_t sgqa_abi_version(void) { return SGQA_ABI_VERSION; }
+
+sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns) {
+  g_wait_ns = ns;
+  return SGQA_OK;
+}
+
+sgqa_status sgqa_get_device_error(sgqa_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SGQA_ERR_CUDA;
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof v) != cudaSuccess) return SGQA_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return SGQA_ERR_CUDA;
+  return static_cast<sgqa_status>(v);
+}
+
+sgqa_status sgqa_selftest_wait_timeout(uint64_t limit_ns, sgqa_stream_t stream) {
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  k_selftest_wait<<<1, 1, 0, st>>>(limit_ns, nullptr);
+  return cudaGetLastError() == cudaSuccess ? SGQA_OK : SGQA_ERR_CUDA;
+}
+
+size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64_t ctx_len, int32_t batch) {
+  Prm p;
+  if (check_params(prm, p) != SGQA_OK || T < 0 || ctx_len < 1) return 0;
+  const int64_t max_cand = (ctx_len - 1) / p.B;
+  switch (op) {
+    case SGQA_OP_INDEX_TOPK:
+    case SGQA_OP_PREFILL:
+      return std::max<size_t>(256, index_ws_bytes(p, std::min<int64_t>(std::max<int64_t>(T, 1), kIndexChunkRows), max_cand));
+    case SGQA_OP_ATTN:
+      return 256;
+    case SGQA_OP_DECODE: {
+      if (batch < 1 || batch > kMaxBatch) return 0;
+      const size_t sc = index_ws_bytes(p, batch, max_cand);
+      const int nsplit = 32;
+      const size_t po = align_up((size_t)p.G * batch * nsplit * 16 * 192 * 4, 256);
+      const size_t pml = align_up((size_t)p.G * batch * nsplit * 16 * 2 * 4, 256);
+      return sc + po + pml;
+    }
+  }
+  return 0;
+}
+
+sgqa_status sgqa_build_block_index(const sgqa_params* prm, const void* k_proxy, int64_t ctx_cap, int64_t tok_begin,
+                                   int64_t tok_end, void* k_blk, int64_t nb_cap, sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  if (!k_proxy || !k_blk || ctx_cap < 0 || tok_begin < 0 || tok_end < tok_begin || tok_end > ctx_cap)
+    return SGQA_ERR_INVALID_ARGUMENT;
+  if (!aligned16(k_proxy) || !aligned16(k_blk)) return SGQA_ERR_INVALID_ARGUMENT;
+  if (tok_end == tok_begin) return SGQA_OK;
+  const int64_t b0 = tok_begin / p.B, b1 = cdiv(tok_end, p.B);
+  if (b1 > nb_cap) return SGQA_ERR_INVALID_ARGUMENT;
+  K1Args a{};
+  a.k_proxy = static_cast<const __nv_bfloat16*>(k_proxy);
+  a.k_blk = static_cast<__nv_bfloat16*>(k_blk);
+  a.ctx_cap = ctx_cap;
+  a.nb_cap = nb_cap;
+  a.tok_end = tok_end;
+  a.blk_begin = b0;
+  a.n_blocks = b1 - b0;
+  a.G = p.G;
+  a.P = p.P;
+  a.B = p.B;
+  SGQA_CUDA_OK(launch_k1(a, reinterpret_cast<cudaStream_t>(stream)));
+  return SGQA_OK;
+}
+
+sgqa_status sgqa_index_topk(const sgqa_params* prm, const void* q_proxy, int64_t T, int64_t q_start, const void* k_blk,
+                            int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes,
+                            sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  if (!q_proxy || !k_blk || !sel_idx || !sel_cnt || T < 0 || q_start < 0) return SGQA_ERR_INVALID_ARGUMENT;
+  if (T == 0) return SGQA_OK;
+  if (!ws) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(q_proxy) || !aligned16(k_blk)) return SGQA_ERR_INVALID_ARGUMENT;
+  const int64_t max_cand = (q_start + T - 1) / p.B;
+  if (max_cand > nb_cap || (q_start + T - 1) / p.B > (int64_t)INT32_MAX) return SGQA_ERR_INVALID_ARGUMENT;
+  return run_index_topk(p, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgqa_status sgqa_sparse_attn_fwd(const sgqa_params* prm, const void* q, const void* k, const void* v, int64_t ctx_cap,
+                                 const void* gate, const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T,
+                                 int64_t q_start, void* out, float* lse, int32_t dense_mode, sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  if (!q || !k || !v || !gate || !out || T < 0 || q_start < 0 || ctx_cap < 1) return SGQA_ERR_INVALID_ARGUMENT;
+  if (!dense_mode && (!sel_idx || !sel_cnt)) return SGQA_ERR_INVALID_ARGUMENT;
+  if (q_start + T > ctx_cap) return SGQA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)p.G * ctx_cap > (int64_t)INT32_MAX) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (p.gate_per_dim && !aligned16(gate)))
+    return SGQA_ERR_INVALID_ARGUMENT;
+  if (T == 0) return SGQA_OK;
+  return run_attention(p, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, dense_mode ? 1 : 0,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, const void* v, const void* gate,
+                         const void* q_proxy, const void* k_proxy, int64_t ctx_cap, int64_t T, int64_t q_start,
+                         void* k_blk, int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse,
+                         void* ws, size_t ws_bytes, sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  if (!q || !k || !v || !gate || !q_proxy || !k_proxy || !k_blk || !sel_idx || !sel_cnt || !out)
+    return SGQA_ERR_INVALID_ARGUMENT;
+  if (T < 0 || q_start < 0 || q_start + T > ctx_cap) return SGQA_ERR_INVALID_ARGUMENT;
+  if (T == 0) return SGQA_OK;
+  if (cdiv(q_start + T, p.B) > nb_cap) return SGQA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)p.G * ctx_cap > (int64_t)INT32_MAX) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (!ws) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  s = sgqa_build_block_index(prm, k_proxy, ctx_cap, q_start, q_start + T, k_blk, nb_cap, stream);
+  if (s != SGQA_OK) return s;
+  s = sgqa_index_topk(prm, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, ws_bytes, stream);
+  if (s != SGQA_OK) return s;
+  return sgqa_sparse_attn_fwd(prm, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, 0, stream);
+}
+
+sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len, const int64_t* kv_off,
+                        const void* q, const void* q_proxy, const void* gate, const void* k_cache, const void* v_cache,
+                        const void* k_proxy_cache, void* k_blk_cache, int64_t total, int32_t* sel_idx,
+                        int32_t* sel_cnt, void* out, float* lse, void* ws, size_t ws_bytes, sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (batch < 1 || batch > kMaxBatch || !ctx_len || !kv_off) return SGQA_ERR_INVALID_ARGUMENT;
+  if (!q || !q_proxy || !gate || !k_cache || !v_cache || !k_blk_cache || !sel_idx || !sel_cnt || !out)
+    return SGQA_ERR_INVALID_ARGUMENT;
+  if (total < 1 || total % p.B != 0) return SGQA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)p.G * total > (int64_t)INT32_MAX) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  int64_t max_len = 0;
+  for (int i = 0; i < batch; ++i) {
+    if (ctx_len[i] < 1 || kv_off[i] < 0 || kv_off[i] % p.B != 0 || kv_off[i] + ctx_len[i] > total)
+      return SGQA_ERR_INVALID_ARGUMENT;
+    max_len = std::max(max_len, ctx_len[i]);
+  }
+  const size_t need = sgqa_workspace_bytes(prm, SGQA_OP_DECODE, 1, max_len, batch);
+  if (!ws || ws_bytes < need) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(ws) || !aligned16(q_proxy) || !aligned16(k_blk_cache) || !aligned16(q) || !aligned16(out))
+    return SGQA_ERR_INVALID_ARGUMENT;
+  const int64_t nb_total = total / p.B;
+  const int64_t max_cand = (max_len - 1) / p.B;
+  const int64_t ld = std::max<int64_t>(4, (int64_t)align_up((size_t)max_cand, 4));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  float* scores = reinterpret_cast<float*>(w);
+  w += index_ws_bytes(p, batch, max_cand);
+  const int nsplit = 32;
+  float* part_o = reinterpret_cast<float*>(w);
+  w += align_up((size_t)p.G * batch * nsplit * 16 * 192 * 4, 256);
+  float* part_ml = reinterpret_cast<float*>(w);
+
+  // 1. rebuild the block holding each new token
+  if (k_proxy_cache) {
+    if (!aligned16(k_proxy_cache)) return SGQA_ERR_INVALID_ARGUMENT;
+    K1SeqArgs a1{};
+    a1.k_proxy = static_cast<const __nv_bfloat16*>(k_proxy_cache);
+    a1.k_blk = static_cast<__nv_bfloat16*>(k_blk_cache);
+    a1.total = total;
+    a1.G = p.G;
+    a1.P = p.P;
+    a1.B = p.B;
+    a1.batch = batch;
+    for (int i = 0; i < batch; ++i) {
+      a1.ctx_len[i] = ctx_len[i];
+      a1.kv_off[i] = kv_off[i];
+    }
+    const int n_vec = p.G * batch * (p.P / 8);
+    k1_block_index_seq<<<(unsigned)cdiv(n_vec, 256), 256, 0, st>>>(a1);
+    SGQA_CUDA_OK(cudaGetLastError());
+  }
+  // 2. indexer scores (matrix-vector per sequence and group)
+  if (max_cand > 0) {
+    K2dArgs a2{};
+    a2.qp = static_cast<const __nv_bfloat16*>(q_proxy);
+    a2.kblk = static_cast<const __nv_bfloat16*>(k_blk_cache);
+    a2.scores = scores;
+    a2.ld = ld;
+    a2.nb_total = nb_total;
+    a2.G = p.G;
+    a2.P = p.P;
+    a2.B = p.B;
+    a2.batch = batch;
+    a2.rows_per_cta = 1024;
+    for (int i = 0; i < batch; ++i) {
+      a2.ctx_len[i] = ctx_len[i];
+      a2.kv_off[i] = kv_off[i];
+    }
+    dim3 grid((unsigned)cdiv(max_cand, a2.rows_per_cta), (unsigned)(p.G * batch));
+    k2d_decode_index<<<grid, 256, 0, st>>>(a2);
+    SGQA_CUDA_OK(cudaGetLastError());
+  }
+  // 3. top-k
+  {
+    K3Args a3{};
+    a3.scores = scores;
+    a3.ld = ld;
+    a3.rows = batch;
+    a3.pos0 = 0;
+    a3.out_row0 = 0;
+    a3.T_out = batch;
+    a3.G = p.G;
+    a3.B = p.B;
+    a3.k = p.k;
+    a3.sel_idx = sel_idx;
+    a3.sel_cnt = sel_cnt;
+    a3.use_pos = 1;
+    for (int i = 0; i < batch; ++i) a3.pos[i] = ctx_len[i] - 1;
+    SGQA_CUDA_OK(launch_k3(a3, max_cand, st));
+  }
+  // 4. split-K attention + combine
+  {
+    K4Args a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.gate = static_cast<const __nv_bfloat16*>(gate);
+    a.kc = static_cast<const __nv_bfloat16*>(k_cache);
+    a.vc = static_cast<const __nv_bfloat16*>(v_cache);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.part_o = part_o;
+    a.part_ml = part_ml;
+    a.rows = batch;
+    a.pos0 = 0;
+    a.ctx_cap = total;
+    a.G = p.G;
+    a.Hg = p.Hg;
+    a.H = p.H;
+    a.B = p.B;
+    a.kcap = p.k;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.dense = 0;
+    a.gate_per_dim = p.gate_per_dim;
+    a.nsplit = nsplit;
+    a.use_pos = 1;
+    a.wait_ns = g_wait_ns;
+    for (int i = 0; i < batch; ++i) {
+      a.pos[i] = ctx_len[i] - 1;
+      a.kv_off[i] = kv_off[i];
+    }
+    const bool tma = p.B >= 8;
+    CUtensorMap tk{}, tv{};
+    if (tma) {
+      const uint64_t rowsz = (uint64_t)p.G * total;
+      if (!make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, 64, 3, rowsz, 128, 384, 64, 3, p.B))
+        return SGQA_ERR_CUDA;
+      if (!make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, 64, 3, rowsz, 128, 384, 64, 3, p.B))
+        return SGQA_ERR_CUDA;
+    }
+    SGQA_CUDA_OK(launch_k4(a, tk, tv, (int64_t)p.G * batch * nsplit, tma, st));
+    K4CombineArgs c{};
+    c.part_o = part_o;
+    c.part_ml = part_ml;
+    c.gate = a.gate;
+    c.out = a.out;
+    c.lse = lse;
+    c.rows = batch;
+    c.G = p.G;
+    c.Hg = p.Hg;
+    c.H = p.H;
+    c.nsplit = nsplit;
+    c.gate_per_dim = p.gate_per_dim;
+    const int64_t warps = (int64_t)p.G * batch * p.Hg;
+    k4_combine<<<(unsigned)cdiv(warps * 32, 256), 256, 0, st>>>(c);
+    SGQA_CUDA_OK(cudaGetLastError());
+  }
+  return SGQA_OK;
+}
+
+}  // extern "C"

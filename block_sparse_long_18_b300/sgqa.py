@@ -1,0 +1,267 @@
+"""Python binding of the Sparse GQA C ABI (include/sgqa.h).
+
+Argument marshalling only: every step of the layer runs in the CUDA library
+``libsgqa.so`` (built from ``csrc/`` by ``build.py``).  Torch tensors supply device
+memory and the current CUDA stream.  Importing this module fails loudly when the library
+has not been built; there is no other code path.
+
+The functions carry the C names and raise :class:`SgqaError` on any status but
+``SGQA_OK``.  Layouts are the ABI's:
+
+  q, gate       [T, H, D] bf16          k, v            [G, C, D] bf16
+  q_proxy       [G, T, P] bf16          k_proxy         [G, C, P] bf16
+  k_blk         [G, NB, P] bf16         sel_idx         [G, T, k] int32, sel_cnt [G, T]
+  out           [T, H, D] bf16          lse             [T, H] fp32
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsgqa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libsgqa.so is not built ({LIB_PATH}); run `python -m block_sparse_long_18_b300.build`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+STATUS = {
+    0: "SGQA_OK",
+    1: "SGQA_ERR_INVALID_ARGUMENT",
+    2: "SGQA_ERR_UNSUPPORTED_SHAPE",
+    3: "SGQA_ERR_WORKSPACE_TOO_SMALL",
+    4: "SGQA_ERR_CUDA",
+    5: "SGQA_ERR_DEVICE_TIMEOUT",
+    6: "SGQA_ERR_DEVICE_BOUNDS",
+}
+SGQA_OP_INDEX_TOPK, SGQA_OP_PREFILL, SGQA_OP_DECODE, SGQA_OP_ATTN = 1, 2, 3, 4
+
+# Every symbol include/sgqa.h declares.
+EXPORTS = (
+    "sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
+    "sgqa_workspace_bytes", "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout",
+    "sgqa_status_string", "sgqa_abi_version",
+)
+
+
+class SgqaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)} ({_lib.sgqa_status_string(code).decode()})")
+
+
+class Params(ctypes.Structure):
+    _fields_ = [
+        ("num_kv_groups", ctypes.c_int32),
+        ("heads_per_group", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("proxy_dim", ctypes.c_int32),
+        ("block_size", ctypes.c_int32),
+        ("top_k_blocks", ctypes.c_int32),
+        ("gate_per_dim", ctypes.c_int32),
+        ("softmax_scale", ctypes.c_float),
+    ]
+
+
+def params(G=4, Hg=16, D=192, P=256, B=8, k=512, gate_per_dim=1, scale=0.0) -> Params:
+    """Layer constants; the defaults are the pages' (phantomic12 entry: 64 heads in 4 KV
+    groups, head_dim 192, topk 512, proxy_dim 256; ai4snews item: block size 8)."""
+    return Params(G, Hg, D, P, B, k, gate_per_dim, scale)
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_PP = ctypes.POINTER(Params)
+_lib.sgqa_status_string.restype = ctypes.c_char_p
+_lib.sgqa_status_string.argtypes = [ctypes.c_int]
+_lib.sgqa_abi_version.restype = ctypes.c_int32
+_lib.sgqa_abi_version.argtypes = []
+_lib.sgqa_build_block_index.argtypes = [_PP, _P, _I64, _I64, _I64, _P, _I64, _P]
+_lib.sgqa_index_topk.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.sgqa_sparse_attn_fwd.argtypes = [_PP, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, ctypes.c_int32, _P]
+_lib.sgqa_prefill.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P,
+                              ctypes.c_size_t, _P]
+_lib.sgqa_decode.argtypes = [_PP, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
+                             ctypes.c_size_t, _P]
+_lib.sgqa_workspace_bytes.restype = ctypes.c_size_t
+_lib.sgqa_workspace_bytes.argtypes = [_PP, ctypes.c_int32, _I64, _I64, ctypes.c_int32]
+_lib.sgqa_get_device_error.argtypes = [_P]
+_lib.sgqa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+_lib.sgqa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _P]
+for _f in ("sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
+           "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout"):
+    getattr(_lib, _f).restype = ctypes.c_int
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SgqaError(code, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor | None, dtype, name: str, shape=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+BF16, I32, F32 = torch.bfloat16, torch.int32, torch.float32
+
+
+def abi_version() -> int:
+    return int(_lib.sgqa_abi_version())
+
+
+def sgqa_workspace_bytes(prm: Params, op: int, T: int, ctx_len: int, batch: int = 1) -> int:
+    return int(_lib.sgqa_workspace_bytes(ctypes.byref(prm), op, T, ctx_len, batch))
+
+
+def sgqa_build_block_index(prm: Params, k_proxy, tok_begin: int, tok_end: int, k_blk, stream=None):
+    G, C, P = k_proxy.shape
+    _check(_lib.sgqa_build_block_index(ctypes.byref(prm), _dev(k_proxy, BF16, "k_proxy"), C, tok_begin, tok_end,
+                                       _dev(k_blk, BF16, "k_blk"), k_blk.shape[1], _stream(stream)),
+           "sgqa_build_block_index")
+
+
+def sgqa_index_topk(prm: Params, q_proxy, q_start: int, k_blk, sel_idx, sel_cnt, ws, stream=None):
+    G, T, P = q_proxy.shape
+    _check(_lib.sgqa_index_topk(ctypes.byref(prm), _dev(q_proxy, BF16, "q_proxy"), T, q_start,
+                                _dev(k_blk, BF16, "k_blk"), k_blk.shape[1],
+                                _dev(sel_idx, I32, "sel_idx", (G, T, prm.top_k_blocks)),
+                                _dev(sel_cnt, I32, "sel_cnt", (G, T)), _dev(ws, torch.uint8, "ws"), ws.numel(),
+                                _stream(stream)), "sgqa_index_topk")
+
+
+def sgqa_sparse_attn_fwd(prm: Params, q, k, v, gate, sel_idx, sel_cnt, q_start: int, out, lse=None,
+                         dense_mode: bool = False, stream=None):
+    T = q.shape[0]
+    _check(_lib.sgqa_sparse_attn_fwd(ctypes.byref(prm), _dev(q, BF16, "q"), _dev(k, BF16, "k"), _dev(v, BF16, "v"),
+                                     k.shape[1], _dev(gate, BF16, "gate"), _dev(sel_idx, I32, "sel_idx"),
+                                     _dev(sel_cnt, I32, "sel_cnt"), T, q_start, _dev(out, BF16, "out"),
+                                     _dev(lse, F32, "lse"), 1 if dense_mode else 0, _stream(stream)),
+           "sgqa_sparse_attn_fwd")
+
+
+def sgqa_prefill(prm: Params, q, k, v, gate, q_proxy, k_proxy, q_start: int, k_blk, sel_idx, sel_cnt, out, lse, ws,
+                 stream=None):
+    T = q.shape[0]
+    _check(_lib.sgqa_prefill(ctypes.byref(prm), _dev(q, BF16, "q"), _dev(k, BF16, "k"), _dev(v, BF16, "v"),
+                             _dev(gate, BF16, "gate"), _dev(q_proxy, BF16, "q_proxy"), _dev(k_proxy, BF16, "k_proxy"),
+                             k.shape[1], T, q_start, _dev(k_blk, BF16, "k_blk"), k_blk.shape[1],
+                             _dev(sel_idx, I32, "sel_idx"), _dev(sel_cnt, I32, "sel_cnt"), _dev(out, BF16, "out"),
+                             _dev(lse, F32, "lse"), _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
+           "sgqa_prefill")
+
+
+def sgqa_decode(prm: Params, ctx_len, kv_off, q, q_proxy, gate, k_cache, v_cache, k_proxy_cache, k_blk_cache,
+                sel_idx, sel_cnt, out, lse, ws, stream=None):
+    batch = len(ctx_len)
+    cl = (ctypes.c_int64 * batch)(*[int(x) for x in ctx_len])
+    ko = (ctypes.c_int64 * batch)(*[int(x) for x in kv_off])
+    _check(_lib.sgqa_decode(ctypes.byref(prm), batch, cl, ko, _dev(q, BF16, "q"), _dev(q_proxy, BF16, "q_proxy"),
+                            _dev(gate, BF16, "gate"), _dev(k_cache, BF16, "k_cache"), _dev(v_cache, BF16, "v_cache"),
+                            _dev(k_proxy_cache, BF16, "k_proxy_cache"), _dev(k_blk_cache, BF16, "k_blk_cache"),
+                            k_cache.shape[1], _dev(sel_idx, I32, "sel_idx"), _dev(sel_cnt, I32, "sel_cnt"),
+                            _dev(out, BF16, "out"), _dev(lse, F32, "lse"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+                            _stream(stream)), "sgqa_decode")
+
+
+def sgqa_get_device_error(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the sticky device error code."""
+    return int(_lib.sgqa_get_device_error(_stream(stream)))
+
+
+def sgqa_set_wait_timeout_ns(ns: int):
+    _check(_lib.sgqa_set_wait_timeout_ns(int(ns)), "sgqa_set_wait_timeout_ns")
+
+
+def sgqa_selftest_wait_timeout(limit_ns: int, stream=None):
+    _check(_lib.sgqa_selftest_wait_timeout(int(limit_ns), _stream(stream)), "sgqa_selftest_wait_timeout")
+
+
+# ---------------------------------------------------------------------------------------
+# Convenience layer: allocate outputs and workspace with torch, then call the ABI.
+# ---------------------------------------------------------------------------------------
+
+@dataclass
+class PrefillResult:
+    out: torch.Tensor
+    lse: torch.Tensor
+    sel_idx: torch.Tensor
+    sel_cnt: torch.Tensor
+    k_blk: torch.Tensor
+
+
+class PrefillPlan:
+    """Preallocated outputs and workspace for repeated prefill calls of one shape."""
+
+    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda", ws_bytes: int | None = None):
+        self.prm, self.T, self.ctx_cap, self.q_start = prm, T, ctx_cap, q_start
+        G, H, D, P, B, k = (prm.num_kv_groups, prm.num_kv_groups * prm.heads_per_group, prm.head_dim, prm.proxy_dim,
+                            prm.block_size, prm.top_k_blocks)
+        nb = (ctx_cap + B - 1) // B
+        self.k_blk = torch.zeros((G, nb, P), dtype=BF16, device=device)
+        self.sel_idx = torch.empty((G, T, k), dtype=I32, device=device)
+        self.sel_cnt = torch.empty((G, T), dtype=I32, device=device)
+        self.out = torch.empty((T, H, D), dtype=BF16, device=device)
+        self.lse = torch.empty((T, H), dtype=F32, device=device)
+        need = sgqa_workspace_bytes(prm, SGQA_OP_PREFILL, T, q_start + T)
+        self.ws = torch.empty((max(need, ws_bytes or 0),), dtype=torch.uint8, device=device)
+
+    def run(self, q, k, v, gate, q_proxy, k_proxy, stream=None) -> PrefillResult:
+        sgqa_prefill(self.prm, q, k, v, gate, q_proxy, k_proxy, self.q_start, self.k_blk, self.sel_idx, self.sel_cnt,
+                     self.out, self.lse, self.ws, stream)
+        return PrefillResult(self.out, self.lse, self.sel_idx, self.sel_cnt, self.k_blk)
+
+
+def prefill(prm: Params, q, k, v, gate, q_proxy, k_proxy, q_start: int = 0, k_blk=None) -> PrefillResult:
+    """One prefill of the layer on device tensors; allocates outputs and workspace."""
+    plan = PrefillPlan(prm, q.shape[0], k.shape[1], q_start, device=q.device)
+    if k_blk is not None:
+        plan.k_blk = k_blk
+    return plan.run(q, k, v, gate, q_proxy, k_proxy)
+
+
+class HostPrefill:
+    """End-to-end prefill from HOST (pinned) tensors: copies the inputs to the device on
+    one stream, runs the layer, and copies the output back.  Device buffers are kept
+    between calls."""
+
+    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda"):
+        self.prm = prm
+        self.plan = PrefillPlan(prm, T, ctx_cap, q_start, device)
+        G, H, D, P = prm.num_kv_groups, prm.num_kv_groups * prm.heads_per_group, prm.head_dim, prm.proxy_dim
+        mk = lambda *s: torch.empty(s, dtype=BF16, device=device)
+        self.d = dict(q=mk(T, H, D), k=mk(G, ctx_cap, D), v=mk(G, ctx_cap, D), gate=mk(T, H, D), q_proxy=mk(G, T, P),
+                      k_proxy=mk(G, ctx_cap, P))
+        self.out_host = torch.empty((T, H, D), dtype=BF16, pin_memory=True)
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.d.values())
+
+    def d2h_bytes(self) -> int:
+        return self.out_host.numel() * self.out_host.element_size()
+
+    def run(self, host: dict, stream=None) -> torch.Tensor:
+        for name, t in self.d.items():
+            t.copy_(host[name], non_blocking=True)
+        d = self.d
+        self.plan.run(d["q"], d["k"], d["v"], d["gate"], d["q_proxy"], d["k_proxy"], stream)
+        self.out_host.copy_(self.plan.out, non_blocking=True)
+        return self.out_host

@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI: the library loads, exports exactly what include/sgqa.h
+declares, and rejects bad arguments with the documented status codes before any kernel
+is enqueued (no GPU is needed for these paths)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_long_18_b300 import build
+
+    build.build()
+    from block_sparse_long_18_b300 import sgqa
+
+    return sgqa
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "sgqa.h")).read()
+    return sorted(set(re.findall(r"SGQA_API\s+[\w\s\*]+?\b(sgqa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_binding_exports(lib):
+    assert _declared() == sorted(lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = set(re.findall(r"\bT\s+(sgqa_\w+)", out))
+    assert set(_declared()) == exported
+    for name in _declared():
+        assert hasattr(lib._lib, name)
+
+
+def test_abi_version(lib):
+    assert lib.abi_version() == 1
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib._lib.sgqa_status_string(code)
+    assert lib._lib.sgqa_status_string(99) == b"unknown status"
+
+
+def _call_build(lib, prm, kp=1 << 12, ctx=64, b=0, e=64, kb=1 << 12, nb=8):
+    return lib._lib.sgqa_build_block_index(ctypes.byref(prm) if prm is not None else None,
+                                           ctypes.c_void_p(kp), ctx, b, e, ctypes.c_void_p(kb), nb, None)
+
+
+def test_validation_codes(lib):
+    prm = lib.params(G=1, Hg=4, k=8)
+    assert _call_build(lib, None) == 1                                   # null params
+    assert _call_build(lib, prm, kp=0) == 1                               # null tensor
+    assert _call_build(lib, prm, b=10, e=5) == 1                          # inverted range
+    assert _call_build(lib, prm, e=65) == 1                               # past ctx_cap
+    assert _call_build(lib, prm, nb=7) == 1                               # blocks beyond nb_cap
+    assert _call_build(lib, prm, kp=(1 << 12) + 2) == 1                   # misaligned
+    assert _call_build(lib, lib.params(G=1, Hg=4, k=8, D=128)) == 2       # head_dim
+    assert _call_build(lib, lib.params(G=1, Hg=32, k=8)) == 2             # heads per group
+    assert _call_build(lib, lib.params(G=1, Hg=4, k=8, B=3)) == 2         # block size
+    assert _call_build(lib, lib.params(G=1, Hg=4, k=8, P=96)) == 2        # proxy dim
+    assert _call_build(lib, lib.params(G=1, Hg=4, k=0)) == 1              # k
+    assert _call_build(lib, prm, b=5, e=5) == 0                           # empty range: nothing to do
+
+
+def test_index_topk_validation(lib):
+    prm = lib.params(G=1, Hg=4, k=8)
+    f = lib._lib.sgqa_index_topk
+    P = ctypes.c_void_p
+    a = P(1 << 12)
+    # workspace missing / too small
+    assert f(ctypes.byref(prm), a, 256, 0, a, 32, a, a, None, 0, None) == 3
+    assert f(ctypes.byref(prm), a, 256, 0, a, 32, a, a, a, 16, None) == 3
+    # candidates beyond nb_cap
+    assert f(ctypes.byref(prm), a, 256, 0, a, 16, a, a, a, 1 << 20, None) == 1
+    # T = 0 is a no-op
+    assert f(ctypes.byref(prm), a, 0, 0, a, 32, a, a, a, 1 << 20, None) == 0
+
+
+def test_decode_validation(lib):
+    prm = lib.params(G=1, Hg=4, k=8)
+    P = ctypes.c_void_p
+    a = P(1 << 12)
+    cl = (ctypes.c_int64 * 2)(100, 50)
+    off_bad = (ctypes.c_int64 * 2)(0, 3)       # not a multiple of B
+    off_ok = (ctypes.c_int64 * 2)(0, 104)
+    f = lib._lib.sgqa_decode
+    assert f(ctypes.byref(prm), 2, cl, off_bad, a, a, a, a, a, None, a, 160, a, a, a, None, a, 1 << 24, None) == 1
+    assert f(ctypes.byref(prm), 2, cl, off_ok, a, a, a, a, a, None, a, 150, a, a, a, None, a, 1 << 24, None) == 1
+    assert f(ctypes.byref(prm), 0, cl, off_ok, a, a, a, a, a, None, a, 160, a, a, a, None, a, 1 << 24, None) == 1
+    assert f(ctypes.byref(prm), 2, cl, off_ok, a, a, a, a, a, None, a, 160, a, a, a, None, a, 16, None) == 3
+
+
+def test_workspace_sizes(lib):
+    prm = lib.params()
+    # 128K prefill: one pass of 8,192 rows x 4 groups x 16,384 fp32 candidates
+    ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL, 131072, 131072)
+    assert ws == 4 * 8192 * 16384 * 4
+    assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 8) > 0
+    assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 0) == 0
+    assert lib.sgqa_workspace_bytes(lib.params(B=3), lib.SGQA_OP_PREFILL, 16, 16) == 0

@@ -1,0 +1,270 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the same seeded
+inputs.  Selections (and the block index) must match bit for bit; attention outputs
+within the tolerance stated in parity_util.  Large workloads are checked on sampled rows
+(plus the edge rows of the method) in the launch configuration the benchmark times."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from block_sparse_long_18_b300 import inputs as gen
+from parity_util import LSE_ABS, check_outputs, sample_rows, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def sg():
+    from block_sparse_long_18_b300 import build
+
+    build.build()
+    from block_sparse_long_18_b300 import sgqa
+
+    assert torch.cuda.is_available()
+    return sgqa
+
+
+def _prm(sg, wl, gate_per_dim=1):
+    return sg.params(G=wl.G, Hg=wl.Hg, D=wl.D, P=wl.P, B=wl.B, k=wl.k, gate_per_dim=gate_per_dim)
+
+
+def _to_cuda(inp):
+    for name in ("q", "k", "v", "gate", "q_proxy", "k_proxy"):
+        setattr(inp, name, getattr(inp, name).cuda())
+    return inp
+
+
+def _gpu_prefill(sg, inp, wl, prm, gate=None):
+    plan = sg.PrefillPlan(prm, wl.T, wl.C, wl.q_start)
+    if wl.q_start > 0:  # blocks of the cached prefix, built once before the chunk
+        sg.sgqa_build_block_index(prm, inp.k_proxy, 0, wl.q_start, plan.k_blk)
+    res = plan.run(inp.q, inp.k, inp.v, inp.gate if gate is None else gate, inp.q_proxy, inp.k_proxy)
+    torch.cuda.synchronize()
+    assert sg.sgqa_get_device_error() == 0
+    return res
+
+
+def _check_prefill(inp, wl, res, rows, groups=None, gate_per_dim=1, gate_rows_all=None, check_blocks=True,
+                   kb_oracle=None, attn_rows=None):
+    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k, gate_per_dim=gate_per_dim)
+    nb = (wl.C + wl.B - 1) // wl.B
+    if kb_oracle is None:
+        kb_oracle = oracle.block_index(u16(inp.k_proxy), wl.B, 0, wl.C)
+    if check_blocks:
+        assert np.array_equal(u16(res.k_blk)[:, :nb], kb_oracle), "block index differs"
+    K, V = u16(inp.k), u16(inp.v)
+    rows = np.asarray(rows, dtype=np.int64)
+    attn_rows = rows if attn_rows is None else np.asarray(attn_rows, dtype=np.int64)
+    stats = []
+    for g in (range(wl.G) if groups is None else groups):
+        pos = wl.q_start + rows
+        grp = np.full(len(rows), g, np.int32)
+        sel, cnt = oracle.select(d, pos, grp, u16(inp.q_proxy[g][torch.as_tensor(rows, device=inp.q_proxy.device)]),
+                                 kb_oracle)
+        gsel = res.sel_idx[g].cpu().numpy()[rows]
+        gcnt = res.sel_cnt[g].cpu().numpy()[rows]
+        assert np.array_equal(gcnt, cnt), f"group {g}: sel_cnt differs"
+        bad = np.argwhere(np.any(gsel != sel, axis=1))
+        assert bad.size == 0, f"group {g}: selection differs at rows {rows[bad[:5, 0]].tolist()}"
+        if attn_rows.size == 0:
+            continue
+        ai = np.searchsorted(rows, attn_rows)
+        hs = slice(g * wl.Hg, (g + 1) * wl.Hg)
+        ar = torch.as_tensor(attn_rows, device=inp.q.device)
+        q_rows = u16(inp.q[ar][:, hs])
+        gsrc = inp.gate if gate_rows_all is None else gate_rows_all
+        gate_rows = u16(gsrc[ar][:, hs])
+        out, lse = oracle.attention(d, pos[ai], grp[ai], q_rows, gate_rows, K, V, sel[ai], cnt[ai])
+        stats.append(check_outputs(u16(res.out[ar][:, hs]), out, f"group {g} out"))
+        glse = res.lse[ar][:, hs].cpu().numpy()
+        assert np.max(np.abs(glse - lse)) <= LSE_ABS, f"group {g}: lse max err {np.max(np.abs(glse - lse))}"
+    return stats
+
+
+# ---------------------------------------------------------------------------------------
+# small and ragged cases: every row checked
+# ---------------------------------------------------------------------------------------
+
+SMALL = [
+    dict(T=300, G=2, Hg=16, B=8, k=8),                    # ragged T, several tiles, G>1
+    dict(T=129, G=1, Hg=16, B=8, k=5, q_start=200),       # chunk with a cached prefix
+    dict(T=64, G=1, Hg=4, B=8, k=1),                      # k = 1: own block only
+    dict(T=7, G=1, Hg=4, B=8, k=4),                       # T < B
+    dict(T=1, G=1, Hg=4, B=8, k=4),                       # single token
+    dict(T=520, G=1, Hg=2, B=1, k=64),                    # token-level (B = 1) reference form
+    dict(T=300, G=1, Hg=16, B=16, k=6),                   # B = 16
+    dict(T=200, G=1, Hg=8, B=4, k=9),                     # B = 4 (cp.async loader)
+    dict(T=260, G=1, Hg=1, B=8, k=7, P=64),               # P = 64, single head
+    dict(T=333, G=2, Hg=16, B=8, k=40, P=128, planted=True),
+]
+
+
+@pytest.mark.parametrize("case", SMALL, ids=[f"T{c['T']}_B{c['B']}_k{c['k']}_G{c['G']}" for c in SMALL])
+def test_prefill_small_all_rows(sg, case):
+    wl = gen.small_workload(**case)
+    inp = _to_cuda(gen.make_inputs(wl, seed=3))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    _check_prefill(inp, wl, res, np.arange(wl.T))
+
+
+def test_prefill_tiny_config_all_rows(sg):
+    """The tiny workload: T = 2,048, 1 group x 4 heads, k = 32 blocks, every row."""
+    wl = gen.WORKLOADS["tiny"]
+    inp = _to_cuda(gen.make_inputs(wl, seed=0))
+    res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
+    stats = _check_prefill(inp, wl, res, np.arange(wl.T))
+    assert stats[0]["n"] == wl.T * wl.Hg * wl.D
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_prefill_tiny_other_seeds(sg, seed):
+    wl = gen.WORKLOADS["tiny"]
+    inp = _to_cuda(gen.make_inputs(wl, seed=seed))
+    res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
+    _check_prefill(inp, wl, res, np.arange(wl.T))
+
+
+def test_per_head_gate(sg):
+    wl = gen.small_workload(T=200, G=2, Hg=16, B=8, k=6)
+    inp = _to_cuda(gen.make_inputs(wl, seed=5))
+    gate_h = inp.gate[:, :, 0].contiguous()                      # [T, H]
+    prm = _prm(sg, wl, gate_per_dim=0)
+    res = _gpu_prefill(sg, inp, wl, prm, gate=gate_h)
+    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k, gate_per_dim=0)
+    kb = oracle.block_index(u16(inp.k_proxy), wl.B, 0, wl.C)
+    rows = np.arange(wl.T)
+    for g in range(wl.G):
+        sel, cnt = oracle.select(d, rows, np.full(wl.T, g, np.int32), u16(inp.q_proxy[g]), kb)
+        hs = slice(g * wl.Hg, (g + 1) * wl.Hg)
+        out, _ = oracle.attention(d, rows, np.full(wl.T, g, np.int32), u16(inp.q[:, hs]), u16(gate_h[:, hs]),
+                                  u16(inp.k), u16(inp.v), sel, cnt)
+        check_outputs(u16(res.out[:, hs]), out, "per-head gate")
+
+
+def test_dense_mode_equals_dense_attention(sg):
+    wl = gen.small_workload(T=400, G=2, Hg=16, B=8, k=4)
+    inp = _to_cuda(gen.make_inputs(wl, seed=6))
+    prm = _prm(sg, wl)
+    out = torch.empty_like(inp.q)
+    lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device="cuda")
+    dummy_idx = torch.zeros((wl.G, wl.T, wl.k), dtype=torch.int32, device="cuda")
+    dummy_cnt = torch.zeros((wl.G, wl.T), dtype=torch.int32, device="cuda")
+    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, dummy_idx, dummy_cnt, 0, out, lse, dense_mode=True)
+    torch.cuda.synchronize()
+    assert sg.sgqa_get_device_error() == 0
+    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k)
+    rows = np.arange(wl.T)
+    for g in range(wl.G):
+        hs = slice(g * wl.Hg, (g + 1) * wl.Hg)
+        ref, ref_lse = oracle.attention(d, rows, np.full(wl.T, g, np.int32), u16(inp.q[:, hs]), u16(inp.gate[:, hs]),
+                                        u16(inp.k), u16(inp.v), dense=True)
+        check_outputs(u16(out[:, hs]), ref, "dense")
+        assert np.max(np.abs(lse[:, hs].cpu().numpy() - ref_lse)) <= LSE_ABS
+
+
+def test_separate_stages_equal_fused_prefill(sg):
+    """build_block_index + index_topk + sparse_attn_fwd called one by one give the same
+    bytes as the fused prefill entry."""
+    wl = gen.small_workload(T=700, G=2, Hg=16, B=8, k=12, planted=True)
+    inp = _to_cuda(gen.make_inputs(wl, seed=7))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    kb = torch.zeros_like(res.k_blk)
+    sg.sgqa_build_block_index(prm, inp.k_proxy, 0, wl.C, kb)
+    idx = torch.empty_like(res.sel_idx)
+    cnt = torch.empty_like(res.sel_cnt)
+    ws = torch.empty(sg.sgqa_workspace_bytes(prm, sg.SGQA_OP_INDEX_TOPK, wl.T, wl.T), dtype=torch.uint8, device="cuda")
+    sg.sgqa_index_topk(prm, inp.q_proxy, 0, kb, idx, cnt, ws)
+    out = torch.empty_like(inp.q)
+    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, idx, cnt, 0, out)
+    torch.cuda.synchronize()
+    assert torch.equal(kb, res.k_blk) and torch.equal(idx, res.sel_idx) and torch.equal(cnt, res.sel_cnt)
+    assert torch.equal(out, res.out)
+
+
+def test_small_workspace_many_passes(sg):
+    """A workspace that holds only 128 rows forces many indexer/top-k passes; the result
+    must not change."""
+    wl = gen.small_workload(T=1000, G=2, Hg=16, B=8, k=16, planted=True)
+    inp = _to_cuda(gen.make_inputs(wl, seed=8))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    ld = ((wl.T - 1) // wl.B + 3) // 4 * 4
+    ws = torch.empty(wl.G * 128 * ld * 4, dtype=torch.uint8, device="cuda")
+    idx = torch.empty_like(res.sel_idx)
+    cnt = torch.empty_like(res.sel_cnt)
+    sg.sgqa_index_topk(prm, inp.q_proxy, 0, res.k_blk, idx, cnt, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, res.sel_idx) and torch.equal(cnt, res.sel_cnt)
+
+
+# ---------------------------------------------------------------------------------------
+# error paths on the device (no fault: bounded waits and checked indices)
+# ---------------------------------------------------------------------------------------
+
+def test_bounded_wait_times_out_cleanly(sg):
+    assert sg.sgqa_get_device_error() == 0
+    sg.sgqa_selftest_wait_timeout(2_000_000)   # 2 ms on a barrier nothing arrives at
+    assert sg.sgqa_get_device_error() == 5     # SGQA_ERR_DEVICE_TIMEOUT
+    assert sg.sgqa_get_device_error() == 0     # cleared
+    # the context is still usable
+    wl = gen.small_workload(T=64, G=1, Hg=4, B=8, k=3)
+    inp = _to_cuda(gen.make_inputs(wl, seed=9))
+    res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
+    _check_prefill(inp, wl, res, np.arange(wl.T))
+
+
+def test_out_of_range_selection_is_reported_not_read(sg):
+    wl = gen.small_workload(T=128, G=1, Hg=16, B=8, k=4)
+    inp = _to_cuda(gen.make_inputs(wl, seed=10))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    idx = res.sel_idx.clone()
+    idx[0, 100, 0] = 1_000_000        # far past the cache
+    idx[0, 101, 0] = -7
+    out = torch.empty_like(inp.q)
+    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, idx, res.sel_cnt, 0, out)
+    assert sg.sgqa_get_device_error() == 6     # SGQA_ERR_DEVICE_BOUNDS
+    # rows without a bad index are unaffected
+    assert torch.equal(out[:100], res.out[:100]) and torch.equal(out[102:], res.out[102:])
+
+
+# ---------------------------------------------------------------------------------------
+# full-size workloads (sampled rows)
+# ---------------------------------------------------------------------------------------
+
+def test_l32k_all_selections_and_sampled_attention(sg):
+    wl = gen.WORKLOADS["l32k"]
+    inp = gen.make_inputs(wl, seed=0, device="cuda")
+    res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
+    attn_rows = sample_rows(wl.T, 1024, seed=0, B=wl.B, k=wl.k)
+    _check_prefill(inp, wl, res, np.arange(wl.T), attn_rows=attn_rows)
+    del inp, res
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_l128k_sampled_rows(sg):
+    """The benchmark's workload and launch configuration (fused prefill, default workspace)."""
+    wl = gen.WORKLOADS["l128k"]
+    inp = gen.make_inputs(wl, seed=0, device="cuda")
+    res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
+    rows = sample_rows(wl.T, 256, seed=1, B=wl.B, k=wl.k)
+    _check_prefill(inp, wl, res, rows)
+    del inp, res
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def test_chunk1m_sampled_rows(sg):
+    wl = gen.WORKLOADS["chunk1m"]
+    inp = gen.make_inputs(wl, seed=0, device="cuda")
+    res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
+    rows = sample_rows(wl.T, 96, seed=2, B=wl.B, k=wl.k, q_start=wl.q_start)
+    _check_prefill(inp, wl, res, rows)
+    del inp, res
+    gc.collect()
+    torch.cuda.empty_cache()
