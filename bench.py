@@ -1,0 +1,418 @@
+#!/usr/bin/env python3
+"""Benchmark of the Sparse GQA layer: prefill tokens/s per layer at 128K tokens on B300,
+with the roofline fraction of each stage.
+
+One step = one prefill of the whole layer over one batch of synthetic input (block index
+-> indexer + top-k -> gated sparse attention) for T = 131,072 query tokens, 4 KV groups x
+16 heads, head_dim 192, proxy_dim 256, block 8, top-k 512 blocks.  Inputs are resident in
+HBM when the timed region starts; L2 is flushed (a 256 MB write, twice the L2 size)
+before every step, outside the step's event pair.  The three stages are called through
+the C ABI one after another on one stream with CUDA events between them (the same kernel
+sequence as the fused sgqa_prefill entry), so each stage's device time comes from the
+timed steps themselves.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sgqa|reference]
+
+Under torchrun each rank runs its own layer on its own seeded input (weak scaling, no
+collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline per stage"
+HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)) or None, "measured"
+    except Exception:
+        return HBM_FALLBACK_GBS, BF16_FALLBACK_TFS, 1400.0, "fallback"
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic work of each stage (what the method must move or compute)
+# ---------------------------------------------------------------------------------------
+
+def work_model(wl):
+    T, q0, B, k, G, H, D, P = wl.T, wl.q_start, wl.B, wl.k, wl.G, wl.H, wl.D, wl.P
+    t = np.arange(q0, q0 + T, dtype=np.int64)
+    bt = t // B
+    n = np.minimum(k, bt + 1)                     # kept blocks per (row, group)
+    att = B * (n - 1) + (t % B) + 1               # attended tokens (own block causally cut)
+    sum_bt, sum_n, sum_att = int(bt.sum()), int(n.sum()), int(att.sum())
+    NB_new = (q0 + T + B - 1) // B - q0 // B
+    w = {}
+    w["k1_bytes"] = 2 * G * P * (T + NB_new)
+    w["k2_flop"] = 2 * P * G * sum_bt
+    w["k2_bytes"] = G * P * 2 * (T + (q0 + T) // B) + 4 * G * sum_bt
+    w["k3_bytes"] = 4 * G * sum_bt + 4 * G * sum_n
+    w["k4_flop"] = 4 * D * H * sum_att
+    w["k4_gather_bytes"] = 2 * 2 * D * B * G * sum_n
+    w["k4_bytes"] = w["k4_gather_bytes"] + 3 * 2 * T * H * D + 4 * G * sum_n + 4 * G * T + 4 * T * H
+    w["sum_n"] = sum_n
+    return w
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons, pw = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+                pw.append(float(f[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(pw) if pw else None}
+
+
+# ---------------------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample of the workload
+# ---------------------------------------------------------------------------------------
+
+def cpu_oracle_rate(inp_host, wl, n_rows, seed=0):
+    """Oracle time for n_rows query tokens (all groups: indexer + top-k + attention), plus
+    its block-index pass prorated to those rows.  Returns (tokens/s, seconds, rows, cores)."""
+    import oracle
+
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(wl.T, size=n_rows, replace=False)).astype(np.int64)
+    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k)
+    t0 = time.perf_counter()
+    kb = oracle.block_index(inp_host["k_proxy"], wl.B, 0, wl.C)
+    t_k1 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    for g in range(wl.G):
+        pos = wl.q_start + rows
+        grp = np.full(len(rows), g, np.int32)
+        sel, cnt = oracle.select(d, pos, grp, inp_host["q_proxy"][g][rows], kb)
+        hs = slice(g * wl.Hg, (g + 1) * wl.Hg)
+        oracle.attention(d, pos, grp, inp_host["q"][rows][:, hs], inp_host["gate"][rows][:, hs], inp_host["k"],
+                         inp_host["v"], sel, cnt)
+    t_rows = time.perf_counter() - t0
+    secs = t_rows + t_k1 * len(rows) / wl.T
+    return len(rows) / secs, secs, len(rows), oracle.num_threads()
+
+
+def host_views(inp, rows_needed=None):
+    """uint16 host copies of what the oracle reads (whole K/V/k_proxy; q/gate/q_proxy rows)."""
+    def u16(t):
+        return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    return {"k": u16(inp.k), "v": u16(inp.v), "k_proxy": u16(inp.k_proxy), "q": u16(inp.q), "gate": u16(inp.gate),
+            "q_proxy": u16(inp.q_proxy)}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+
+def run_sgqa(args, rank, world, local_rank):
+    from block_sparse_long_18_b300 import build as _build
+
+    _build.build()
+    from block_sparse_long_18_b300 import inputs as gen
+    from block_sparse_long_18_b300 import sgqa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = gen.WORKLOADS[args.workload]
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    inp = gen.make_inputs(wl, seed=rank, device=dev)
+    prm = sgqa.params(G=wl.G, Hg=wl.Hg, D=wl.D, P=wl.P, B=wl.B, k=wl.k)
+    plan = sgqa.PrefillPlan(prm, wl.T, wl.C, wl.q_start, device=dev)
+    if wl.q_start:
+        sgqa.sgqa_build_block_index(prm, inp.k_proxy, 0, wl.q_start, plan.k_blk)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        sgqa.sgqa_build_block_index(prm, inp.k_proxy, wl.q_start, wl.q_start + wl.T, plan.k_blk, stream)
+        if evs:
+            evs[1].record(stream)
+        sgqa.sgqa_index_topk(prm, inp.q_proxy, wl.q_start, plan.k_blk, plan.sel_idx, plan.sel_cnt, plan.ws, stream)
+        if evs:
+            evs[2].record(stream)
+        sgqa.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, plan.sel_idx, plan.sel_cnt, wl.q_start,
+                                  plan.out, plan.lse, stream=stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    err = sgqa.sgqa_get_device_error()
+    if err:
+        raise RuntimeError(f"device error {err} during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        t_wall0 = time.perf_counter()
+        for s in range(args.steps):
+            flush.fill_(s & 0xFF)
+            step(events[s])
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        torch.distributed.barrier()
+    err = sgqa.sgqa_get_device_error()
+    if err:
+        raise RuntimeError(f"device error {err} in the timed region")
+    stage_ms = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in events])  # [steps, 3]
+    step_ms = stage_ms.sum(axis=1)
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * wl.T / (ms / 1e3)
+
+    # ---- roofline of each stage ----
+    w = work_model(wl)
+    k1_ms, ik_ms, k4_ms = (float(x) for x in stage_ms.mean(axis=0))
+    hbm_bps = hbm * 1e9
+    roof = {
+        "k1_block_index": w["k1_bytes"] / hbm_bps * 1e3,
+        "k2k3_index_topk": max(w["k2_flop"] / (bf16 * 1e12), w["k2_bytes"] / hbm_bps) * 1e3 + w["k3_bytes"] / hbm_bps * 1e3,
+        "k4_sparse_attn": max(w["k4_flop"] / (bf16 * 1e12), w["k4_bytes"] / hbm_bps) * 1e3,
+    }
+    meas = {"k1_block_index": k1_ms, "k2k3_index_topk": ik_ms, "k4_sparse_attn": k4_ms}
+    stages = {kname: {"ms": round(meas[kname], 4), "roofline_ms": round(roof[kname], 4),
+                      "frac": round(roof[kname] / meas[kname], 4)} for kname in meas}
+    stages["k4_sparse_attn"]["tensor_tflops"] = round(w["k4_flop"] / (k4_ms / 1e3) / 1e12, 2)
+    stages["k2k3_index_topk"]["k2_tflop"] = round(w["k2_flop"] / 1e12, 4)
+    layer_roof = sum(roof.values())
+
+    roofline = {
+        "kernel": "k4_sparse_attn",
+        "bound": "hbm",
+        "achieved": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9, 1),
+        "peak": hbm,
+        "unit": "GB/s",
+        "frac": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9 / hbm, 4),
+        "traffic": None,
+        "bytes_per_launch": w["k4_bytes"],
+        "peak_source": peak_src,
+    }
+
+    # ---- end to end through the public API, from pinned host memory ----
+    e2e = None
+    if not args.no_e2e:
+        hp = sgqa.HostPrefill(prm, wl.T, wl.C, wl.q_start, device=dev)
+        if wl.q_start:
+            sgqa.sgqa_build_block_index(prm, inp.k_proxy, 0, wl.q_start, hp.plan.k_blk)
+        host = {name: getattr(inp, name).cpu().pin_memory() for name in hp.d}
+        for _ in range(max(1, min(args.warmup, 2))):
+            hp.run(host)
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for s in range(args.steps):
+            ev[s][0].record(stream)
+            hp.run(host)
+            ev[s][1].record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * wl.T / (e_ms / 1e3), "unit": "tokens/s", "ms_per_step": round(e_ms, 3),
+               "h2d_bytes_per_step": hp.h2d_bytes(), "d2h_bytes_per_step": hp.d2h_bytes(),
+               "api": "HostPrefill.run -> sgqa_prefill"}
+        del hp, host
+
+    # ---- CPU baseline (oracle), rank 0 only ----
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        hv = host_views(inp)
+        rate, secs, nrows, cores = cpu_oracle_rate(hv, wl, n_rows=16)
+        if secs < 8.0:   # grow the sample towards ~15 s of CPU work
+            n2 = int(min(wl.T, max(16, 16 * 15.0 / max(secs, 1e-3))))
+            rate, secs, nrows, cores = cpu_oracle_rate(hv, wl, n_rows=n2, seed=1)
+        cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{nrows} query tokens drawn uniformly from the {wl.name} workload, all {wl.G} groups "
+                         f"(indexer + top-k + attention, fp64) plus the block-index pass prorated; {secs:.1f} s"}
+
+    n_chunks = math.ceil(wl.T / min(wl.T, 8192))
+    launches_per_step = 1 + 2 * n_chunks + 1
+    clocks = clk.summary()
+    out = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{wl.name}: prefill T={wl.T} at q_start={wl.q_start}, context {wl.C}, G={wl.G} x Hg={wl.Hg} "
+                        f"heads, D={wl.D}, P={wl.P}, block {wl.B}, top-k {wl.k} blocks, planted={wl.planted}",
+            "global_batch": 1, "seq_len": wl.T, "parallelism": f"replicas x{world}",
+            "l2": "flushed before every step (256 MB write, outside the step events)",
+            "wall_ms_per_step_incl_flush": round(t_wall * 1e3 / args.steps, 3),
+        },
+        "stages": stages,
+        "layer_roofline_ms": round(layer_roof, 4),
+        "layer_roofline_frac": round(layer_roof / ms, 4),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16_sus, "source": peak_src},
+    }
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ---------------------------------------------------------------------------------------
+
+def run_reference(args, rank, world):
+    from block_sparse_long_18_b300 import inputs as gen
+    import oracle
+
+    wl = gen.WORKLOADS[args.workload]
+    inp = gen.make_inputs(wl, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    hv = host_views(inp)
+    del inp
+    rates, secs_all, n_rows = [], [], 8
+    for s in range(args.warmup + args.steps):
+        rate, secs, nrows, cores = cpu_oracle_rate(hv, wl, n_rows=n_rows, seed=100 + s)
+        if s >= args.warmup:
+            rates.append(rate)
+            secs_all.append(secs)
+    value = float(np.mean(rates))
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "tokens/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(float(np.mean(secs_all)) * 1e3, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": f"{wl.name}: prefill T={wl.T}, context {wl.C}, G={wl.G} x Hg={wl.Hg}, D={wl.D}, "
+                               f"P={wl.P}, block {wl.B}, top-k {wl.k}", "global_batch": 1, "seq_len": wl.T},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle", "cores": oracle.num_threads(),
+                         "sample": f"{n_rows} query tokens per step drawn from the workload, all groups, fp64"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["sgqa", "reference"], default="sgqa")
+    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "chunk1m", "l128k_tail"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_sgqa(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

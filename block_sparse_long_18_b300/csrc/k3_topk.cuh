@@ -120,11 +120,10 @@ __global__ void __launch_bounds__(NT) k3_topk(const __grid_constant__ K3Args a) 
 
   uint32_t prefix = 0, pmask = 0;
   uint32_t need_rem = (uint32_t)need, eq_count = 0;
-  const int shifts[3] = {21, 10, 0};
-  const uint32_t wmasks[3] = {0x7FFu, 0x7FFu, 0x3FFu};
+#pragma unroll
   for (int p = 0; p < 3; ++p) {
-    const int sh = shifts[p];
-    const uint32_t wm = wmasks[p];
+    const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
+    const uint32_t wm = p == 2 ? 0x3FFu : 0x7FFu;
     for (int b = tid; b < NBINS; b += NT) hist[b] = 0;
     __syncthreads();
     for (int tile = 0; tile < n_tiles; ++tile) {

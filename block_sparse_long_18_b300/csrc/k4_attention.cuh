@@ -66,7 +66,9 @@ __device__ __forceinline__ uint32_t k4_off(uint32_t n, uint32_t u) {
   return r * 128 + (((u & 7) ^ (r & 7)) << 4);
 }
 
-template <int NW, int NSTAGE, bool TMA>
+// PIPE: issue the next stage's Q K^T before this stage's softmax and P V (needs a stage
+// of prefetch beyond the two in use, so it pays only with NSTAGE >= 3).
+template <int NW, int NSTAGE, bool TMA, bool PIPE>
 __global__ void __launch_bounds__(NW * 32, 1)
     k4_sparse_attn(const __grid_constant__ K4Args a, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV) {
@@ -173,69 +175,125 @@ __global__ void __launch_bounds__(NW * 32, 1)
   float o[24][4];
 #pragma unroll
   for (int d = 0; d < 24; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+  // m0/m1: reference maxima (log2 units) of rows r = lane/4 and r + 8; they may lag the
+  // true running maxima by up to kLazy so that O is rescaled only when a maximum grows.
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  constexpr float kLazy = 8.f;
   const uint32_t qd = lane & 3;  // column pair within an 8-wide tile
   bool ok = true;
   int64_t issued = s_begin;
 
-  for (int s = 0; s < NSTAGE - 1; ++s)
-    if (s_begin + s < s_end) { issue(s_begin + s); issued = s_begin + s + 1; }
-    else if (!TMA) cp_async_commit();
-
-  for (int64_t s = s_begin; s < s_end; ++s) {
-    if (s + NSTAGE - 1 < s_end) { issue(s + NSTAGE - 1); issued = s + NSTAGE; }
-    else if (!TMA) cp_async_commit();
-    const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
+  auto stage_addr = [&](int64_t s) { return wbase + (uint32_t)((s - s_begin) % NSTAGE) * K4_STAGE; };
+  auto wait_stage = [&](int64_t s) -> bool {
     if (TMA) {
-      if (!mbar_wait(bar0 + 8 * slot, (uint32_t)(((s - s_begin) / NSTAGE) & 1), a.wait_ns)) { ok = false; break; }
-    } else {
-      cp_async_wait<NSTAGE - 1>();
-      __syncwarp();
+      const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
+      return mbar_wait(bar0 + 8 * slot, (uint32_t)(((s - s_begin) / NSTAGE) & 1), a.wait_ns);
     }
-    const uint32_t ks_addr = wbase + slot * K4_STAGE;
-    const uint32_t vs_addr = ks_addr + K4_TILE;
-
-    // ---- S = Q K^T ----
-    float sc[2][4];
+    if (PIPE) cp_async_wait<NSTAGE - 2>();  // every group but the newest NSTAGE-2 has landed
+    else cp_async_wait<NSTAGE - 1>();
+    __syncwarp();
+    return true;
+  };
+  // S = Q K^T for one stage: two n-tiles x 12 k-steps, as four independent chains.
+  auto qk = [&](uint32_t ks_addr, float (&sc)[2][4]) {
+    float acc[2][2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.f;
 #pragma unroll
     for (int kp = 0; kp < 12; kp += 2) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
         uint32_t b0, b1, b2, b3;
         ldsm_x4(ks_addr + k4_off(nt * 8 + (lane & 7), 2 * kp + (lane >> 3)), b0, b1, b2, b3);
-        mma_bf16_16816(sc[nt], qa[kp], b0, b1);
-        mma_bf16_16816(sc[nt], qa[kp + 1], b2, b3);
+        mma_bf16_16816(acc[nt][0], qa[kp], b0, b1);
+        mma_bf16_16816(acc[nt][1], qa[kp + 1], b2, b3);
+      }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[nt][e] = acc[nt][0][e] + acc[nt][1][e];
+  };
+
+  for (int s = 0; s < NSTAGE - 1; ++s)
+    if (s_begin + s < s_end) { issue(s_begin + s); issued = s_begin + s + 1; }
+    else if (!TMA) cp_async_commit();
+
+  float sc[2][4];
+  if (PIPE && s_begin < s_end) {
+    if (wait_stage(s_begin)) qk(stage_addr(s_begin), sc);
+    else ok = false;
+  }
+
+  for (int64_t s = s_begin; ok && s < s_end; ++s) {
+    // prefetch into the slot stage s-1 has released
+    if (s + NSTAGE - 1 < s_end) { issue(s + NSTAGE - 1); issued = s + NSTAGE; }
+    else if (!TMA) cp_async_commit();
+    // scores of the next stage are issued first so their MMAs overlap this stage's softmax
+    float sn[2][4];
+    const bool has_next = PIPE && s + 1 < s_end;
+    if (PIPE) {
+      if (has_next) {
+        if (!wait_stage(s + 1)) { ok = false; break; }
+        qk(stage_addr(s + 1), sn);
+      }
+    } else {
+      if (!wait_stage(s)) { ok = false; break; }
+      qk(stage_addr(s), sc);
+    }
+
+    // ---- scale; mask unused slots, invalid indices and tokens after t ----
+    bool fast = true;  // every block of the stage valid and strictly before the own block
+    for (int bi = 0; bi < bps; ++bi) {
+      const int64_t b = block_of(s * bps + bi);
+      fast = fast && b >= 0 && b < bt;
+    }
+    if (fast) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] *= a.scale_log2;
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int key = nt * 8 + 2 * qd + c;
+          const int64_t b = block_of(s * bps + key / a.B);
+          const bool valid = b >= 0 && b * a.B + (key % a.B) <= t;
+          if (b == -2) report_error(kErrBounds);
+          sc[nt][c] = valid ? sc[nt][c] * a.scale_log2 : -INFINITY;
+          sc[nt][2 + c] = valid ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+        }
       }
     }
 
-    // ---- mask: unused slots, invalid indices, and tokens after t in the own block ----
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const int key = nt * 8 + 2 * qd + c;
-        const int64_t b = block_of(s * bps + key / a.B);
-        const bool valid = b >= 0 && b * a.B + (key % a.B) <= t;
-        if (b == -2 && c == 0 && nt == 0 && lane == 0) report_error(kErrBounds);
-        sc[nt][c] = valid ? sc[nt][c] * a.scale_log2 : -INFINITY;
-        sc[nt][2 + c] = valid ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
-      }
-    }
-
-    // ---- online softmax (rows r = lane/4 and r + 8) ----
+    // ---- online softmax, rows r = lane/4 and r + 8 ----
     float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
     float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0, mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float al0 = fast_exp2(m0 - mu0), al1 = fast_exp2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
+    if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
+      const float al1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
+      l0 *= al0;
+      l1 *= al1;
+#pragma unroll
+      for (int d = 0; d < 24; ++d) {
+        o[d][0] *= al0;
+        o[d][1] *= al0;
+        o[d][2] *= al1;
+        o[d][3] *= al1;
+      }
+      m0 = mn0;
+      m1 = mn1;
+    }
+    const float mu0 = m0 == -INFINITY ? 0.f : m0, mu1 = m1 == -INFINITY ? 0.f : m1;
     float p[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -244,15 +302,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       p[nt][2] = fast_exp2(sc[nt][2] - mu1);
       p[nt][3] = fast_exp2(sc[nt][3] - mu1);
     }
-    l0 = l0 * al0 + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
-    l1 = l1 * al1 + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
-#pragma unroll
-    for (int d = 0; d < 24; ++d) {
-      o[d][0] *= al0;
-      o[d][1] *= al0;
-      o[d][2] *= al1;
-      o[d][3] *= al1;
-    }
+    l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
+    l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);
     uint32_t pa[4];
     pa[0] = pack_bf16(p[0][0], p[0][1]);
     pa[1] = pack_bf16(p[0][2], p[0][3]);
@@ -260,6 +311,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
     pa[3] = pack_bf16(p[1][2], p[1][3]);
 
     // ---- O += P V ----
+    const uint32_t vs_addr = stage_addr(s) + K4_TILE;
 #pragma unroll
     for (int dp = 0; dp < 12; ++dp) {
       const uint32_t mtx = lane >> 3;
@@ -268,7 +320,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
       mma_bf16_16816(o[2 * dp], pa, v0, v1);
       mma_bf16_16816(o[2 * dp + 1], pa, v2, v3);
     }
-    __syncwarp();
+    __syncwarp();  // every lane is done with this stage's slot
+    if (has_next) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = sn[nt][e];
+    }
   }
 
   if (!ok) {

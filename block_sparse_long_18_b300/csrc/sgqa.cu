@@ -111,18 +111,21 @@ int num_sms() {
   return n;
 }
 
-// ---- attention launch configuration (warps per CTA, stages per warp) ----
+// ---- attention launch configuration (warps per CTA, stages per warp, pipelined QK) ----
 struct K4Cfg {
-  int nw, ns;
+  int nw, ns, pipe;
 };
 K4Cfg k4_cfg() {
   static K4Cfg c = [] {
-    K4Cfg d{4, 4};
+    K4Cfg d{8, 2, 0};
     if (const char* e = std::getenv("SGQA_K4_CFG")) {
       int a = 0, b = 0;
-      if (std::sscanf(e, "%dx%d", &a, &b) == 2) {
-        if ((a == 4 && b == 4) || (a == 8 && b == 2) || (a == 6 && b == 3) || (a == 4 && b == 3) || (a == 8 && b == 3))
-          d = K4Cfg{a, b};
+      char pc = 0;
+      const int n = std::sscanf(e, "%dx%d%c", &a, &b, &pc);
+      if (n >= 2) {
+        const int pipe = (n == 3 && pc == 'p') ? 1 : 0;
+        const bool known = (a == 8 && b == 2) || (a == 6 && b == 3) || (a == 4 && b == 4) || (a == 5 && b == 3);
+        if (known) d = K4Cfg{a, b, pipe};
       }
     }
     return d;
@@ -132,31 +135,34 @@ K4Cfg k4_cfg() {
 
 size_t k4_smem(int nw, int ns) { return (size_t)nw * ns * K4_STAGE + (size_t)nw * ns * 8 + 1024; }
 
-template <int NW, int NS, bool TMA>
+template <int NW, int NS, bool TMA, bool PIPE>
 cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
                         cudaStream_t st) {
   const size_t smem = k4_smem(NW, NS);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k4_sparse_attn<NW, NS, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k4_sparse_attn<NW, NS, TMA, PIPE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int64_t grid = cdiv(n_units, NW);
-  k4_sparse_attn<NW, NS, TMA><<<(unsigned)grid, NW * 32, smem, st>>>(a, tk, tv);
+  k4_sparse_attn<NW, NS, TMA, PIPE><<<(unsigned)grid, NW * 32, smem, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_k4(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units, bool tma,
                       cudaStream_t st) {
-  if (!tma) return launch_k4_t<4, 4, false>(a, tk, tv, n_units, st);
+  if (!tma) return launch_k4_t<8, 2, false, false>(a, tk, tv, n_units, st);
   const K4Cfg c = k4_cfg();
-  if (c.nw == 8 && c.ns == 2) return launch_k4_t<8, 2, true>(a, tk, tv, n_units, st);
-  if (c.nw == 6 && c.ns == 3) return launch_k4_t<6, 3, true>(a, tk, tv, n_units, st);
-  if (c.nw == 4 && c.ns == 3) return launch_k4_t<4, 3, true>(a, tk, tv, n_units, st);
-  if (c.nw == 8 && c.ns == 3) return launch_k4_t<8, 3, true>(a, tk, tv, n_units, st);
-  return launch_k4_t<4, 4, true>(a, tk, tv, n_units, st);
+  if (c.nw == 6 && c.ns == 3) return c.pipe ? launch_k4_t<6, 3, true, true>(a, tk, tv, n_units, st)
+                                            : launch_k4_t<6, 3, true, false>(a, tk, tv, n_units, st);
+  if (c.nw == 5 && c.ns == 3) return c.pipe ? launch_k4_t<5, 3, true, true>(a, tk, tv, n_units, st)
+                                            : launch_k4_t<5, 3, true, false>(a, tk, tv, n_units, st);
+  if (c.nw == 4 && c.ns == 4) return c.pipe ? launch_k4_t<4, 4, true, true>(a, tk, tv, n_units, st)
+                                            : launch_k4_t<4, 4, true, false>(a, tk, tv, n_units, st);
+  return c.pipe ? launch_k4_t<8, 2, true, true>(a, tk, tv, n_units, st)
+                : launch_k4_t<8, 2, true, false>(a, tk, tv, n_units, st);
 }
 
 cudaError_t launch_k2(const K2Args& a, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,

@@ -64,6 +64,9 @@ WORKLOADS = {
     "l128k_b1": Workload("l128k_b1", T=131072, C=131072, B=1, k=2048),
     "decode": Workload("decode", T=1, C=0, batch=8, ctx_lo=262144, ctx_hi=1048576),
     "chunk1m": Workload("chunk1m", T=8192, C=1048576, q_start=1048576 - 8192),
+    # the last 16,384 queries of a 128K context: the 128K gather pattern in ~2 GB of HBM
+    # (used for profiler captures, which must stay small)
+    "l128k_tail": Workload("l128k_tail", T=16384, C=131072, q_start=131072 - 16384),
 }
 
 

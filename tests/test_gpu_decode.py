@@ -83,8 +83,11 @@ def test_decode_matches_prefill_last_row(sg):
     prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k)
     plan = sg.PrefillPlan(prm, wl.T, wl.C)
     pre = plan.run(inp.q, inp.k, inp.v, inp.gate, inp.q_proxy, inp.k_proxy)
-    dec_in = gen.Inputs(wl, inp.q[-1:].contiguous(), inp.k, inp.v, inp.gate[-1:].contiguous(),
-                        inp.q_proxy[:, -1:].contiguous(), inp.k_proxy, inp.carry[-1:], None, ctx_len=[wl.T], kv_off=[0])
+    # decode caches hold a whole number of blocks: pad 1500 -> 1504 rows (never attended)
+    pad = lambda x: torch.nn.functional.pad(x, (0, 0, 0, 4)).contiguous()
+    dec_in = gen.Inputs(wl, inp.q[-1:].contiguous(), pad(inp.k), pad(inp.v), inp.gate[-1:].contiguous(),
+                        inp.q_proxy[:, -1:].contiguous(), pad(inp.k_proxy), inp.carry[-1:], None, ctx_len=[wl.T],
+                        kv_off=[0])
     k_blk, sel, cnt, out, lse = _run_decode(sg, dec_in, wl, prm)
     assert torch.equal(sel[:, 0], pre.sel_idx[:, -1]) and torch.equal(cnt[:, 0], pre.sel_cnt[:, -1])
     d = (out[0].float() - pre.out[-1].float()).abs().max().item()
