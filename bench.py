@@ -37,6 +37,12 @@ sys.path.insert(0, ROOT)
 METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline per stage"
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
+# DRAM bytes (read + write) per K4 launch from an ncu capture of the current kernel
+# (profiles/k4_sparse_attn_l128k_tail.md): 7.52 GB for the 65,536 (row, group) units of
+# the l128k_tail workload, scaled to the full 128K launch by kept blocks (x7.88).
+K4_TRAFFIC = {"l128k_tail": 7.517e9, "l128k": 59.2e9}
+K4_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, l128k_tail capture (scaled for l128k)"
+
 
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -262,7 +268,8 @@ def run_sgqa(args, rank, world, local_rank):
         "peak": hbm,
         "unit": "GB/s",
         "frac": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9 / hbm, 4),
-        "traffic": None,
+        "traffic": K4_TRAFFIC.get(wl.name),
+        "traffic_source": K4_TRAFFIC_SOURCE if wl.name in K4_TRAFFIC else None,
         "bytes_per_launch": w["k4_bytes"],
         "peak_source": peak_src,
     }
