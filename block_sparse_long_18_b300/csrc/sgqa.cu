@@ -309,6 +309,28 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
   return SGQA_OK;
 }
 
+// ---- scratch for the allocation-free indexer entry ----
+// A file-scope device array: every GPU that loads the library holds it until exit.  Host
+// code must not pass the symbol itself to a kernel (in host code it names a host-side
+// stand-in); its device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SGQA_NOALLOC_SCRATCH_BYTES];
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices] = {};
+
+sgqa_status noalloc_scratch_address(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SGQA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return SGQA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return SGQA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -409,6 +431,27 @@ sgqa_status sgqa_index_topk(const sgqa_params* prm, const void* q_proxy, int64_t
   const int64_t max_cand = (q_start + T - 1) / p.B;
   if (max_cand > nb_cap || (q_start + T - 1) / p.B > (int64_t)INT32_MAX) return SGQA_ERR_INVALID_ARGUMENT;
   return run_index_topk(p, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, ws_bytes,
+                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+sgqa_status sgqa_index_topk_noalloc(const sgqa_params* prm, const void* q_proxy, int64_t T, int64_t q_start,
+                                    const void* k_blk, int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt,
+                                    sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  if (!q_proxy || !k_blk || !sel_idx || !sel_cnt || T < 0 || q_start < 0) return SGQA_ERR_INVALID_ARGUMENT;
+  if (T == 0) return SGQA_OK;
+  if (!aligned16(q_proxy) || !aligned16(k_blk)) return SGQA_ERR_INVALID_ARGUMENT;
+  const int64_t max_cand = (q_start + T - 1) / p.B;
+  if (max_cand > nb_cap || max_cand > (int64_t)INT32_MAX) return SGQA_ERR_INVALID_ARGUMENT;
+  // the smallest pass must fit in the fixed scratch array
+  if (index_ws_bytes(p, std::min<int64_t>(T, 128), max_cand) > (size_t)SGQA_NOALLOC_SCRATCH_BYTES)
+    return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  void* ws = nullptr;
+  s = noalloc_scratch_address(&ws);
+  if (s != SGQA_OK) return s;
+  return run_index_topk(p, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, SGQA_NOALLOC_SCRATCH_BYTES,
                         reinterpret_cast<cudaStream_t>(stream));
 }
 

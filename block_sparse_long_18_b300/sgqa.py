@@ -43,7 +43,7 @@ SGQA_OP_INDEX_TOPK, SGQA_OP_PREFILL, SGQA_OP_DECODE, SGQA_OP_ATTN = 1, 2, 3, 4
 EXPORTS = (
     "sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
     "sgqa_workspace_bytes", "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout",
-    "sgqa_status_string", "sgqa_abi_version",
+    "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc",
 )
 
 
@@ -81,6 +81,7 @@ _lib.sgqa_abi_version.restype = ctypes.c_int32
 _lib.sgqa_abi_version.argtypes = []
 _lib.sgqa_build_block_index.argtypes = [_PP, _P, _I64, _I64, _I64, _P, _I64, _P]
 _lib.sgqa_index_topk.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P, ctypes.c_size_t, _P]
+_lib.sgqa_index_topk_noalloc.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P]
 _lib.sgqa_sparse_attn_fwd.argtypes = [_PP, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, ctypes.c_int32, _P]
 _lib.sgqa_prefill.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P,
                               ctypes.c_size_t, _P]
@@ -91,7 +92,7 @@ _lib.sgqa_workspace_bytes.argtypes = [_PP, ctypes.c_int32, _I64, _I64, ctypes.c_
 _lib.sgqa_get_device_error.argtypes = [_P]
 _lib.sgqa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 _lib.sgqa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _P]
-for _f in ("sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
+for _f in ("sgqa_build_block_index", "sgqa_index_topk", "sgqa_index_topk_noalloc", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
            "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout"):
     getattr(_lib, _f).restype = ctypes.c_int
 
@@ -146,6 +147,21 @@ def sgqa_index_topk(prm: Params, q_proxy, q_start: int, k_blk, sel_idx, sel_cnt,
                                 _dev(sel_idx, I32, "sel_idx", (G, T, prm.top_k_blocks)),
                                 _dev(sel_cnt, I32, "sel_cnt", (G, T)), _dev(ws, torch.uint8, "ws"), ws.numel(),
                                 _stream(stream)), "sgqa_index_topk")
+
+
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def sgqa_index_topk_noalloc(prm: Params, q_proxy, q_start: int, k_blk, sel_idx, sel_cnt, stream=None):
+    """sgqa_index_topk for callers that cannot allocate: the library's own fixed scratch
+    array (NOALLOC_SCRATCH_BYTES per device) replaces the workspace.  Calls that overlap on
+    the GPU race on that array."""
+    G, T, P = q_proxy.shape
+    _check(_lib.sgqa_index_topk_noalloc(ctypes.byref(prm), _dev(q_proxy, BF16, "q_proxy"), T, q_start,
+                                        _dev(k_blk, BF16, "k_blk"), k_blk.shape[1],
+                                        _dev(sel_idx, I32, "sel_idx", (G, T, prm.top_k_blocks)),
+                                        _dev(sel_cnt, I32, "sel_cnt", (G, T)), _stream(stream)),
+           "sgqa_index_topk_noalloc")
 
 
 def sgqa_sparse_attn_fwd(prm: Params, q, k, v, gate, sel_idx, sel_cnt, q_start: int, out, lse=None,

@@ -183,6 +183,32 @@ SGQA_API sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const in
                         int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse, void* ws, size_t ws_bytes,
                         sgqa_stream_t stream);
 
+/* ---------------------------------------------------------------------------------
+ * Indexer + top-k without a caller-provided workspace.  No counterpart on the pages: it
+ * exists for callers that cannot allocate device memory at the point of the call, for
+ * example an inference engine that reserves nearly all of HBM for its KV cache at
+ * start-up and hands its kernels only input and output pointers, or a plugin interface
+ * whose contract passes tensors but no scratch buffer.
+ *
+ * Same operation, arguments and results as sgqa_index_topk, minus ws / ws_bytes.  The
+ * score scratch is a file-scope device array of SGQA_NOALLOC_SCRATCH_BYTES inside this
+ * library; every GPU that loads the library holds it until the process exits.  The call
+ * allocates nothing (no cudaMalloc / cudaFree, no allocating library routine).
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     with that device current); make that first call before any stream capture.
+ *   - All calls share the array and it keeps the last call's contents; nothing in it has
+ *     to start at zero (every score the top-k reads is written earlier in the same call).
+ *     Calls that overlap on the GPU (different streams, or another thread) race on it.
+ *   - A request whose smallest pass (min(T, 128) query rows x G groups x the candidate
+ *     count of the last row, rounded up to 4, in fp32) does not fit in the array returns
+ *     SGQA_ERR_WORKSPACE_TOO_SMALL before anything is launched; larger requests that do
+ *     fit run in as many passes as needed.
+ * ------------------------------------------------------------------------------- */
+#define SGQA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+SGQA_API sgqa_status sgqa_index_topk_noalloc(const sgqa_params* prm, const void* q_proxy, int64_t T, int64_t q_start,
+                                             const void* k_blk, int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt,
+                                             sgqa_stream_t stream);
+
 /* Workspace bytes needed by `op` for T query rows ending at context length ctx_len
  * (decode: the largest ctx_len of the batch).  Returns 0 for an invalid request. */
 SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64_t ctx_len, int32_t batch);
