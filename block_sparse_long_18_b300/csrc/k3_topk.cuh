@@ -7,14 +7,18 @@
 // slots go to the strictly earlier blocks in order (score descending, block index
 // descending); -0 and +0 compare equal; the kept set is written in ascending order.
 //
-// One CTA per (group, query row).  Scores are mapped to order-preserving unsigned keys;
-// a radix select over 11/11/10-bit digits (shared-memory histograms, block-wide suffix
-// search) finds the key of the (k-1)-th best candidate and how many candidates equal to
-// it are kept; it stops early once a digit bucket is taken whole.  Equal keys are taken
-// from the largest index down by ranking them in index order.  The final pass compacts
-// the kept indices in ascending order with one block-wide scan per tile of candidates.
-// Rows up to NT*PER candidates keep their keys in registers (one pass over global
-// memory); longer rows (contexts past 128K tokens at B = 8) stream tiles per pass.
+// One CTA of NT threads per (group, query row).  Scores are mapped to order-preserving
+// unsigned keys.  Thread `tid` holds, for j = 0..PER/4-1, the four consecutive candidates
+// 4*(j*NT + tid) .. +3, so every load is one coalesced float4 per thread and each group j
+// covers 4*NT consecutive indices.  A radix select over 11/11/10-bit digits (shared-memory
+// histograms, block-wide suffix search; the first pass needs no prefix test) finds the key
+// of the (k-1)-th best candidate and how many candidates equal to it are kept, stopping as
+// soon as a digit bucket is kept whole.  Equal keys are taken from the largest index down:
+// they are ranked in index order and the first `skip` of them are passed over.  The
+// compaction writes the kept indices in ascending order: per group j each warp scans its
+// lanes' counts, one block-wide scan over the (j, warp) totals places the warps.  Rows up to
+// NT*PER candidates keep their keys in registers; longer rows (contexts past 128K tokens at
+// B = 8) are processed in tiles of NT*PER, re-read for every pass.
 #pragma once
 #include "ptx.cuh"
 
@@ -40,25 +44,27 @@ __device__ __forceinline__ uint32_t score_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Inclusive warp scan.
+__device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
+  const uint32_t lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= (uint32_t)o) v += t;
+  }
+  return v;
+}
+
 template <int NT>
 __device__ __forceinline__ uint32_t k3_block_excl_scan(uint32_t v, uint32_t* warp_tot, uint32_t& total) {
   constexpr int NW = NT / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += t;
-  }
+  const uint32_t incl = warp_incl_scan(v);
   if (lane == 31) warp_tot[warp] = incl;
   __syncthreads();
   if (warp == 0) {
     uint32_t t = lane < NW ? warp_tot[lane] : 0u;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      uint32_t s = __shfl_up_sync(0xffffffffu, t, o);
-      if (lane >= o) t += s;
-    }
+    t = warp_incl_scan(t);
     if (lane < NW) warp_tot[lane] = t;
   }
   __syncthreads();
@@ -69,133 +75,204 @@ __device__ __forceinline__ uint32_t k3_block_excl_scan(uint32_t v, uint32_t* war
 }
 
 template <int NT, int PER, bool STREAM>
-__global__ void __launch_bounds__(NT) k3_topk(const __grid_constant__ K3Args a) {
+__global__ void __launch_bounds__(NT, STREAM ? 1 : 2) k3_topk(const __grid_constant__ K3Args a) {
   constexpr int NBINS = 2048;
   constexpr int BPT = NBINS / NT;  // bins per thread
+  constexpr int NJ = PER / 4;      // groups of 4 consecutive keys per thread
+  constexpr int NW = NT / 32;
   constexpr int TILE = NT * PER;
-  __shared__ uint32_t hist[NBINS];
-  __shared__ uint32_t warp_tot[NT / 32];
-  __shared__ uint32_t sh_digit, sh_above;
+  __shared__ uint32_t hist2[2][NBINS];  // ping-pong: one is counted while the other is cleared
+  __shared__ uint32_t warp_tot[NW];
+  __shared__ uint32_t wsum[2][NW];
+  __shared__ uint32_t jw_cnt[NJ * NW];  // counts per (group j, warp), then their exclusive scan
+  __shared__ uint32_t sh_digit, sh_above, sh_eq;
 
   const int64_t r = blockIdx.x;
   const int64_t g = r / a.rows;
   const int64_t i = r % a.rows;
   const int64_t pos = a.use_pos ? a.pos[i] : a.pos0 + i;
   const int64_t bt = pos / a.B;
-  const int64_t n = bt;                 // candidates 0 .. bt-1
+  const int64_t n = bt;  // candidates 0 .. bt-1
   const int need = a.k - 1;
   int32_t* out = a.sel_idx + ((g * a.T_out) + a.out_row0 + i) * a.k;
   const float* row = a.scores + (g * a.rows + i) * a.ld;
   const int tid = threadIdx.x;
+  const uint32_t lane = tid & 31, warp = tid >> 5;
 
   if (n <= need) {  // every causal block is kept
     for (int64_t j = tid; j < a.k; j += NT) out[j] = j < n ? (int32_t)j : (j == n ? (int32_t)bt : -1);
     if (tid == 0) a.sel_cnt[g * a.T_out + a.out_row0 + i] = (int32_t)(n + 1);
     return;
   }
+  if (need == 0) {  // k = 1: the own block alone
+    if (tid == 0) {
+      out[0] = (int32_t)bt;
+      a.sel_cnt[g * a.T_out + a.out_row0 + i] = 1;
+    }
+    return;
+  }
 
   const int n_tiles = STREAM ? (int)((n + TILE - 1) / TILE) : 1;
+  // candidate index of key e of group j in tile `tile`
+  auto kidx = [&](int tile, int j, int e) -> int32_t { return tile * TILE + 4 * (j * NT + tid) + e; };
   uint32_t key[PER];
   auto load_tile = [&](int tile) {
-    const int64_t base = (int64_t)tile * TILE + (int64_t)tid * PER;
 #pragma unroll
-    for (int j = 0; j < PER; j += 4) {
-      if (base + j + 3 < n) {
-        float4 f = __ldg(reinterpret_cast<const float4*>(row + base + j));
-        key[j] = score_key(f.x);
-        key[j + 1] = score_key(f.y);
-        key[j + 2] = score_key(f.z);
-        key[j + 3] = score_key(f.w);
+    for (int j = 0; j < NJ; ++j) {
+      const int32_t b = kidx(tile, j, 0);
+      if (b + 3 < n) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(row + b));
+        key[4 * j] = score_key(f.x);
+        key[4 * j + 1] = score_key(f.y);
+        key[4 * j + 2] = score_key(f.z);
+        key[4 * j + 3] = score_key(f.w);
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) key[j + e] = (base + j + e < n) ? score_key(__ldg(row + base + j + e)) : 0u;
+        for (int e = 0; e < 4; ++e) key[4 * j + e] = (b + e < n) ? score_key(__ldg(row + b + e)) : 0u;
       }
     }
   };
   if (tid == 0) {
     sh_digit = 0;
     sh_above = 0;
+    sh_eq = 0;
   }
   if (!STREAM) load_tile(0);
 
+  // Slots past the last candidate hold key 0.  Every finite score maps to a key of at
+  // least 0x007FFFFF (the key of -inf), so key 0 only ever lands in bin 0 of the first
+  // digit, below every real candidate; since there are more candidates than keys to keep,
+  // the search never reaches it and no pass needs an index test.
+  for (int b = tid; b < NBINS; b += NT) {
+    hist2[0][b] = 0;
+    hist2[1][b] = 0;
+  }
+  __syncthreads();
   uint32_t prefix = 0, pmask = 0;
   uint32_t need_rem = (uint32_t)need, eq_count = 0;
 #pragma unroll
   for (int p = 0; p < 3; ++p) {
     const int sh = p == 0 ? 21 : (p == 1 ? 10 : 0);
     const uint32_t wm = p == 2 ? 0x3FFu : 0x7FFu;
-    for (int b = tid; b < NBINS; b += NT) hist[b] = 0;
-    __syncthreads();
+    uint32_t* hist = hist2[p & 1];
     for (int tile = 0; tile < n_tiles; ++tile) {
       if (STREAM) load_tile(tile);
-      const int64_t base = (int64_t)tile * TILE + (int64_t)tid * PER;
 #pragma unroll
-      for (int j = 0; j < PER; ++j)
-        if (base + j < n && (key[j] & pmask) == prefix) atomicAdd(&hist[(key[j] >> sh) & wm], 1u);
+      for (int q = 0; q < PER; ++q) {
+        const uint32_t kk = key[q];
+        if (p == 0 || (kk & pmask) == prefix) atomicAdd(&hist[(kk >> sh) & wm], 1u);
+      }
     }
-    __syncthreads();
-    // find the digit holding the need_rem-th largest matching key
+    __syncthreads();  // (1) histogram complete
+    // digit holding the need_rem-th largest matching key: thread tid owns bins
+    // [tid*BPT, tid*BPT + BPT); warp sums go to smem and every thread adds up the warps
+    // above its own, so no second scan round is needed.
+    uint32_t h[BPT];
     uint32_t loc = 0;
 #pragma unroll
-    for (int b = 0; b < BPT; ++b) loc += hist[tid * BPT + b];
-    uint32_t total;
-    const uint32_t excl = k3_block_excl_scan<NT>(loc, warp_tot, total);
-    uint32_t cum = total - excl - loc;  // keys in bins above this thread's bins
+    for (int b = 0; b < BPT; ++b) {
+      h[b] = hist[tid * BPT + b];
+      loc += h[b];
+    }
+    // the other buffer is free: clear it for the next pass
+    if (p < 2) {
+#pragma unroll
+      for (int b = 0; b < BPT; ++b) hist2[(p + 1) & 1][tid * BPT + b] = 0;
+    }
+    const uint32_t incl = warp_incl_scan(loc);
+    const uint32_t wtot = __shfl_sync(0xffffffffu, incl, 31);
+    if (lane == 31) wsum[p & 1][warp] = wtot;
+    __syncthreads();  // (2) warp sums visible
+    uint32_t above_warp = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+      if (w > (int)warp) above_warp += wsum[p & 1][w];
+    uint32_t cum = above_warp + (wtot - incl);  // keys in bins above this thread's bins
 #pragma unroll
     for (int b = BPT - 1; b >= 0; --b) {
-      const uint32_t h = hist[tid * BPT + b];
-      if (cum < need_rem && cum + h >= need_rem) {
+      if (cum < need_rem && cum + h[b] >= need_rem) {
         sh_digit = (uint32_t)(tid * BPT + b);
         sh_above = cum;
+        sh_eq = h[b];
       }
-      cum += h;
+      cum += h[b];
     }
-    __syncthreads();
+    __syncthreads();  // (3) digit visible
     const uint32_t d = sh_digit;
     need_rem -= sh_above;
-    eq_count = hist[d];
+    eq_count = sh_eq;
     prefix |= d << sh;
     pmask |= wm << sh;
-    __syncthreads();
     if (need_rem == eq_count) break;  // the whole bucket is kept: no tie to break
   }
 
   // ---- compaction in ascending index order ----
-  const uint32_t skip = eq_count - need_rem;  // equal keys passed over, smallest indices first
+  // A key is kept if its masked value exceeds the prefix, or equals it and its rank among
+  // the equal keys (in index order) is at least `skip`.
+  const uint32_t skip = eq_count - need_rem;
   uint32_t out_base = 0, tie_base = 0;
   for (int tile = 0; tile < n_tiles; ++tile) {
     if (STREAM) load_tile(tile);
-    const int64_t base = (int64_t)tile * TILE + (int64_t)tid * PER;
-    uint32_t c_gt = 0, c_eq = 0;
+    // per (j, lane): packed counts (greater << 16 | equal) of its 4 keys, scanned per warp
+    uint32_t wex[NJ];
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      if (base + j < n) {
-        const uint32_t kh = key[j] & pmask;
-        c_gt += kh > prefix;
-        c_eq += kh == prefix;
+    for (int j = 0; j < NJ; ++j) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t kh = key[4 * j + e] & pmask;
+        c += kh > prefix ? (1u << 16) : (kh == prefix ? 1u : 0u);
       }
+      const uint32_t inc = warp_incl_scan(c);
+      wex[j] = inc - c;
+      if (lane == 31) jw_cnt[j * NW + warp] = inc;
     }
-    uint32_t total;
-    const uint32_t ex = k3_block_excl_scan<NT>((c_gt << 16) | c_eq, warp_tot, total);
-    uint32_t ties_before = tie_base + (ex & 0xFFFFu);
-    // kept ties before this thread within this tile: those of global rank >= skip
-    const uint32_t kept_prev = tie_base > skip ? tie_base - skip : 0u;
-    uint32_t o = out_base + (ex >> 16) + (ties_before > skip ? ties_before - skip : 0u) - kept_prev;
+    __syncthreads();
+    // exclusive scan over the NJ*NW (group, warp) totals in index order (j major)
+    if (warp == 0) {
+      constexpr int PERL = (NJ * NW + 31) / 32;
+      uint32_t v[PERL];
+      uint32_t s = 0;
 #pragma unroll
-    for (int j = 0; j < PER; ++j) {
-      if (base + j < n) {
-        const uint32_t kh = key[j] & pmask;
+      for (int q = 0; q < PERL; ++q) {
+        const int idx = lane * PERL + q;
+        v[q] = idx < NJ * NW ? jw_cnt[idx] : 0u;
+        s += v[q];
+      }
+      const uint32_t inc = warp_incl_scan(s);
+      uint32_t run = inc - s;
+#pragma unroll
+      for (int q = 0; q < PERL; ++q) {
+        const int idx = lane * PERL + q;
+        if (idx < NJ * NW) jw_cnt[idx] = run;
+        run += v[q];
+      }
+      if (lane == 31) warp_tot[0] = inc;  // tile total
+    }
+    __syncthreads();
+    const uint32_t tile_tot = warp_tot[0];
+    const uint32_t kept_prev = tie_base > skip ? tie_base - skip : 0u;  // ties kept by earlier tiles
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+      const uint32_t ex = jw_cnt[j * NW + warp] + wex[j];  // packed counts before this lane's group j
+      uint32_t ties_before = tie_base + (ex & 0xFFFFu);
+      uint32_t o = out_base + (ex >> 16) + (ties_before > skip ? ties_before - skip : 0u) - kept_prev;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int32_t idx = (int32_t)kidx(tile, j, e);
+        const uint32_t kh = key[4 * j + e] & pmask;
         if (kh > prefix) {
-          out[o++] = (int32_t)(base + j);
+          out[o++] = idx;
         } else if (kh == prefix) {
-          if (ties_before >= skip) out[o++] = (int32_t)(base + j);
+          if (ties_before >= skip) out[o++] = idx;
           ++ties_before;
         }
       }
     }
-    const uint32_t t_gt = total >> 16, t_eq = total & 0xFFFFu;
+    const uint32_t t_gt = tile_tot >> 16, t_eq = tile_tot & 0xFFFFu;
     out_base += t_gt + ((tie_base + t_eq > skip) ? (tie_base + t_eq - (tie_base > skip ? tie_base : skip)) : 0u);
     tie_base += t_eq;
+    __syncthreads();  // jw_cnt / warp_tot are rewritten by the next tile
   }
   if (tid == 0) {
     out[need] = (int32_t)bt;

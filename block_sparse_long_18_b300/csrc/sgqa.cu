@@ -21,6 +21,7 @@
 #include "k2d_decode_index.cuh"
 #include "k3_topk.cuh"
 #include "k4_attention.cuh"
+#include "k4tc_attention.cuh"
 
 using namespace sgqa;
 
@@ -272,9 +273,65 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
   return SGQA_OK;
 }
 
+// Which attention kernel serves prefill: the tcgen05 one for blocks of 8 or 16 tokens
+// (the TMA gathers land in whole 1 KB swizzle atoms), the warp-level one otherwise.
+bool use_k4tc(const Prm& p) {
+  static const int forced = [] {
+    const char* e = std::getenv("SGQA_K4_IMPL");
+    return e ? (std::strcmp(e, "mma") == 0 ? 0 : (std::strcmp(e, "tc") == 0 ? 1 : -1)) : -1;
+  }();
+  return forced == 1 && p.B == 8;
+}
+
+cudaError_t launch_k4tc(const K4TArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                        cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k4tc_sparse_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K4T_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t n_units = (int64_t)a.G * a.rows;
+  const int64_t grid = std::min<int64_t>(n_units, num_sms());
+  if (grid <= 0) return cudaSuccess;
+  k4tc_sparse_attn<<<(unsigned)grid, K4T_THREADS, K4T_SMEM, st>>>(a, tq, tk, tv);
+  return cudaGetLastError();
+}
+
 sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void* v, int64_t ctx_cap, const void* gate,
                           const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T, int64_t q_start, void* out,
                           float* lse, int32_t dense, cudaStream_t st) {
+  if (use_k4tc(p)) {
+    K4TArgs a{};
+    a.gate = static_cast<const __nv_bfloat16*>(gate);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.rows = T;
+    a.pos0 = q_start;
+    a.ctx_cap = ctx_cap;
+    a.G = p.G;
+    a.Hg = p.Hg;
+    a.H = p.H;
+    a.B = p.B;
+    a.kcap = p.k;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.dense = dense;
+    a.gate_per_dim = p.gate_per_dim;
+    a.wait_ns = g_wait_ns;
+    CUtensorMap tq, tk, tv;
+    const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
+    if (!make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 64, 3, (uint64_t)T * p.H, 128, 384, 64, 1, 16))
+      return SGQA_ERR_CUDA;
+    // Block-major maps: dims {64, tokens, 3 chunks} with strides {384 B, 128 B}, so one copy
+    // of box {64, 8, 3} lands a block as its three 1 KB atoms.
+    if (!make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, 64, rowsz, 3, 384, 128, 64, 8, 3)) return SGQA_ERR_CUDA;
+    if (!make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, 64, rowsz, 3, 384, 128, 64, 8, 3)) return SGQA_ERR_CUDA;
+    a.block_major = 1;
+    SGQA_CUDA_OK(launch_k4tc(a, tq, tk, tv, st));
+    return SGQA_OK;
+  }
   K4Args a{};
   a.q = static_cast<const __nv_bfloat16*>(q);
   a.gate = static_cast<const __nv_bfloat16*>(gate);
