@@ -75,7 +75,7 @@ __device__ __forceinline__ uint32_t k3_block_excl_scan(uint32_t v, uint32_t* war
 }
 
 template <int NT, int PER, bool STREAM>
-__global__ void __launch_bounds__(NT, STREAM ? 1 : 2) k3_topk(const __grid_constant__ K3Args a) {
+__global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __grid_constant__ K3Args a) {
   constexpr int NBINS = 2048;
   constexpr int BPT = NBINS / NT;  // bins per thread
   constexpr int NJ = PER / 4;      // groups of 4 consecutive keys per thread

@@ -181,10 +181,16 @@ cudaError_t launch_k2(const K2Args& a, const CUtensorMap& ta, const CUtensorMap&
   return cudaGetLastError();
 }
 
+// One CTA per row; the block is the smallest whose registers (32 keys per thread) hold
+// the launch's longest row, so short rows do not pay for empty slots.
 cudaError_t launch_k3(const K3Args& a, int64_t max_cand, cudaStream_t st) {
   const int64_t grid = (int64_t)a.G * a.rows;
   if (grid <= 0) return cudaSuccess;
-  if (max_cand <= kK3RegRow)
+  if (max_cand <= 128 * kK3Per)
+    k3_topk<128, kK3Per, false><<<(unsigned)grid, 128, 0, st>>>(a);
+  else if (max_cand <= 256 * kK3Per)
+    k3_topk<256, kK3Per, false><<<(unsigned)grid, 256, 0, st>>>(a);
+  else if (max_cand <= kK3RegRow)
     k3_topk<kK3Threads, kK3Per, false><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
   else
     k3_topk<kK3Threads, kK3Per, true><<<(unsigned)grid, kK3Threads, 0, st>>>(a);

@@ -268,3 +268,30 @@ def test_chunk1m_sampled_rows(sg):
     del inp, res
     gc.collect()
     torch.cuda.empty_cache()
+
+
+def test_coverage_from_lse_matches_oracle_coverage(sg):
+    """The coverage diagnostic: exp(LSE_sel - LSE_dense) from the GPU equals the oracle's
+    dense-softmax mass on the selected tokens, computed from scratch."""
+    wl = gen.small_workload(T=600, G=2, Hg=16, B=8, k=12, planted=True)
+    inp = _to_cuda(gen.make_inputs(wl, seed=12))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    lse_d = torch.empty_like(res.lse)
+    out = torch.empty_like(inp.q)
+    dummy = torch.zeros((wl.G, wl.T, 1), dtype=torch.int32, device="cuda")
+    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, dummy, dummy[:, :, 0].contiguous(), 0, out, lse_d,
+                            dense_mode=True)
+    torch.cuda.synchronize()
+    cov_gpu = torch.exp(res.lse.double() - lse_d.double()).cpu().numpy()
+    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k)
+    kb = oracle.block_index(u16(inp.k_proxy), wl.B, 0, wl.C)
+    rows = np.arange(wl.T)
+    for g in range(wl.G):
+        grp = np.full(wl.T, g, np.int32)
+        sel, cnt = oracle.select(d, rows, grp, u16(inp.q_proxy[g]), kb)
+        hs = slice(g * wl.Hg, (g + 1) * wl.Hg)
+        _, _, cov = oracle.attention(d, rows, grp, u16(inp.q[:, hs]), u16(inp.gate[:, hs]), u16(inp.k), u16(inp.v),
+                                     sel, cnt, want_coverage=True)
+        np.testing.assert_allclose(cov_gpu[:, hs], cov, atol=3e-3, rtol=0)
+        assert np.all(cov[: 8 * (wl.k - 1)] > 1 - 1e-12)  # rows whose every block is kept
