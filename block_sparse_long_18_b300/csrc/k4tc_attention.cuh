@@ -46,7 +46,7 @@ constexpr uint32_t K4T_Q_OFF = 4 * K4T_KV;
 constexpr uint32_t K4T_P_OFF = K4T_Q_OFF + 2 * K4T_QB;
 constexpr uint32_t K4T_BAR_OFF = K4T_P_OFF + 2 * K4T_PB;
 constexpr uint32_t K4T_SMEM = K4T_BAR_OFF + 1024 + 1024;  // + barriers/scratch + alignment
-constexpr int K4T_THREADS = 192;
+constexpr int K4T_THREADS = 224;  // 7 warps
 constexpr uint32_t K4T_TMEM_COLS = 128;
 // TMEM columns: S buffers 0 and 16; O buffer ob: 32 + 32*ob (d 0..127), +16 (d 64..191)
 
@@ -61,6 +61,8 @@ struct K4TArgs {
   float scale_log2;
   int32_t dense, gate_per_dim;
   int32_t block_major;  // 1: one TMA copy per block lands [3 chunks][8 keys][64] (B = 8)
+  int32_t g_first, g_count;  // groups handled by this launch (one launch per group keeps the
+                             // CTAs of a launch on one group's K/V, which L2 holds)
   uint64_t wait_ns;
 };
 
@@ -121,7 +123,7 @@ struct K4TUnit {
 
 __device__ __forceinline__ K4TUnit k4t_unit(const K4TArgs& a, int64_t u) {
   K4TUnit x;
-  x.g = (int32_t)(u / a.rows);
+  x.g = a.g_first + (int32_t)(u / a.rows);
   x.i = u % a.rows;
   x.t = a.pos0 + x.i;
   x.bt = x.t / a.B;
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const int64_t n_units = (int64_t)a.G * a.rows;
+  const int64_t n_units = (int64_t)a.g_count * a.rows;
   const int bpc = 128 / a.B;  // blocks per chunk
 
   if (threadIdx.x == 0) {
@@ -197,23 +199,28 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------- TMA producer -------------------------------
+  if (warp == 0 || warp == 6) {
+    // ---------------- TMA producers: warp 0 streams Q and K, warp 6 streams V ----------------
+    // Separate streams let K run up to two chunks ahead of V: the next chunk's scores and
+    // softmax overlap the flight of its V tile, which is then held only briefly.
+    const bool is_k = warp == 0;
     uint32_t uc = 0, kc = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
       const K4TUnit x = k4t_unit(a, u);
-      const uint32_t qb = uc & 1;
-      if (lane == 0) {
-        if (uc >= 2) ok = mbar_wait(bar(kQEmpty + qb), ((uc >> 1) - 1) & 1, a.wait_ns, abort_flag);
-        if (ok) {
-          mbar_arrive_expect_tx(bar(kQFull + qb), K4T_QB);
-          for (int r = 0; r < 3; ++r)
-            tma_load_3d(sb0 + K4T_Q_OFF + qb * K4T_QB + r * 2048, &tmQ, bar(kQFull + qb), 0, r,
-                        (int32_t)(x.i * a.H + (int64_t)x.g * a.Hg));
+      if (is_k) {
+        const uint32_t qb = uc & 1;
+        if (lane == 0) {
+          if (uc >= 2) ok = mbar_wait(bar(kQEmpty + qb), ((uc >> 1) - 1) & 1, a.wait_ns, abort_flag);
+          if (ok) {
+            mbar_arrive_expect_tx(bar(kQFull + qb), K4T_QB);
+            for (int r = 0; r < 3; ++r)
+              tma_load_3d(sb0 + K4T_Q_OFF + qb * K4T_QB + r * 2048, &tmQ, bar(kQFull + qb), 0, r,
+                          (int32_t)(x.i * a.H + (int64_t)x.g * a.Hg));
+          }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
       for (int64_t c = 0; c < x.n_ch && ok; ++c, ++kc) {
         const uint32_t slot = kc & 1;
         int64_t blk = -1;
@@ -222,42 +229,36 @@ __global__ void __launch_bounds__(K4T_THREADS, 1)
           if (blk < 0) blk = x.bt;  // unused or bad slot: fetch the own block, masked later
         }
         const int32_t row = (int32_t)((int64_t)x.g * a.ctx_cap + blk * a.B);
-        for (int tsr = 0; tsr < 2 && ok; ++tsr) {  // 0: K, 1: V
-          const int full = (tsr ? kVFull : kKFull) + slot, empty = (tsr ? kVEmpty : kKEmpty) + slot;
-          const uint32_t base = sb0 + (tsr ? K4T_V_OFF : K4T_K_OFF) + slot * K4T_KV;
-          if (lane == 0) {
-            if (kc >= 2) ok = mbar_wait(bar(empty), ((kc >> 1) - 1) & 1, a.wait_ns, abort_flag);
-            if (ok) mbar_arrive_expect_tx(bar(full), K4T_KV);
-          }
-          ok = __shfl_sync(0xffffffffu, ok, 0);
-          if (ok && (int)lane < bpc) {
-            if (a.block_major) {  // one copy: the block's 3 atoms, 3 KB apart per block
-              tma_load_3d(base + lane * 3072, tsr ? &tmV : &tmK, bar(full), 0, row, 0);
-            } else {
-              for (int r = 0; r < 3; ++r)
-                tma_load_3d(base + r * K4T_REGION + lane * a.B * 128, tsr ? &tmV : &tmK, bar(full), 0, r, row);
-            }
-          }
-          __syncwarp();
+        const int full = (is_k ? kKFull : kVFull) + slot, empty = (is_k ? kKEmpty : kVEmpty) + slot;
+        const uint32_t base = sb0 + (is_k ? K4T_K_OFF : K4T_V_OFF) + slot * K4T_KV;
+        if (lane == 0) {
+          if (kc >= 2) ok = mbar_wait(bar(empty), ((kc >> 1) - 1) & 1, a.wait_ns, abort_flag);
+          if (ok) mbar_arrive_expect_tx(bar(full), K4T_KV);
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && (int)lane < bpc) {
+          if (a.block_major) {  // one copy: the block's 3 atoms, 3 KB apart per block
+            tma_load_3d(base + lane * 3072, is_k ? &tmK : &tmV, bar(full), 0, row, 0);
+          } else {
+            for (int r = 0; r < 3; ++r)
+              tma_load_3d(base + r * K4T_REGION + lane * a.B * 128, is_k ? &tmK : &tmV, bar(full), 0, r, row);
+          }
+        }
+        __syncwarp();
       }
     }
     // drain: the latest copies into every buffer land before the CTA leaves
     if (lane == 0) {
-      if (uc > 0) {
-        // the last unit actually issued is uc-1 only when the loop ended normally; wait on
-        // the most recent phase of each buffer that was used at all
+      if (is_k)
         for (uint32_t b = 0; b < 2; ++b)
           if (uc > b) {
             const uint32_t last = ((uc - 1 - b) & ~1u) + b;
             mbar_wait(bar(kQFull + b), (last >> 1) & 1, kDrainLimitNs);
           }
-      }
       for (uint32_t b = 0; b < 2; ++b)
         if (kc > b) {
           const uint32_t last = ((kc - 1 - b) & ~1u) + b;
-          mbar_wait(bar(kKFull + b), (last >> 1) & 1, kDrainLimitNs);
-          mbar_wait(bar(kVFull + b), (last >> 1) & 1, kDrainLimitNs);
+          mbar_wait(bar((is_k ? kKFull : kVFull) + b), (last >> 1) & 1, kDrainLimitNs);
         }
     }
   } else if (warp == 1) {

@@ -297,11 +297,17 @@ cudaError_t launch_k4tc(const K4TArgs& a, const CUtensorMap& tq, const CUtensorM
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int64_t n_units = (int64_t)a.G * a.rows;
-  const int64_t grid = std::min<int64_t>(n_units, num_sms());
+  const int64_t grid = std::min<int64_t>(a.rows, num_sms());
   if (grid <= 0) return cudaSuccess;
-  k4tc_sparse_attn<<<(unsigned)grid, K4T_THREADS, K4T_SMEM, st>>>(a, tq, tk, tv);
-  return cudaGetLastError();
+  for (int g = 0; g < a.G; ++g) {  // one launch per KV group
+    K4TArgs ag = a;
+    ag.g_first = g;
+    ag.g_count = 1;
+    k4tc_sparse_attn<<<(unsigned)grid, K4T_THREADS, K4T_SMEM, st>>>(ag, tq, tk, tv);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void* v, int64_t ctx_cap, const void* gate,
