@@ -425,6 +425,70 @@ def run_sgqa(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------------------------------------------
+# decode step timing (not the headline metric; reported for the decode workload)
+# ---------------------------------------------------------------------------------------
+
+def run_decode(args, local_rank):
+    from block_sparse_long_18_b300 import build as _build
+
+    _build.build()
+    from block_sparse_long_18_b300 import inputs as gen
+    from block_sparse_long_18_b300 import sgqa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = gen.WORKLOADS["decode"]
+    inp = gen.make_decode_inputs(wl, seed=0, device=dev)
+    prm = sgqa.params(G=wl.G, Hg=wl.Hg, D=wl.D, P=wl.P, B=wl.B, k=wl.k)
+    total = inp.k.shape[1]
+    batch = len(inp.ctx_len)
+    k_blk = torch.zeros((wl.G, total // wl.B, wl.P), dtype=torch.bfloat16, device=dev)
+    for L, off in zip(inp.ctx_len, inp.kv_off):
+        sgqa.sgqa_build_block_index(prm, inp.k_proxy, off, off + L - 1, k_blk)
+    sel = torch.empty((wl.G, batch, wl.k), dtype=torch.int32, device=dev)
+    cnt = torch.empty((wl.G, batch), dtype=torch.int32, device=dev)
+    out = torch.empty((batch, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((batch, wl.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(sgqa.sgqa_workspace_bytes(prm, sgqa.SGQA_OP_DECODE, 1, max(inp.ctx_len), batch),
+                     dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        sgqa.sgqa_decode(prm, inp.ctx_len, inp.kv_off, inp.q, inp.q_proxy, inp.gate, inp.k, inp.v, inp.k_proxy,
+                         k_blk, sel, cnt, out, lse, ws)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for s in range(args.steps):
+        flush.fill_(s & 0xFF)
+        ev[s][0].record()
+        step()
+        ev[s][1].record()
+    torch.cuda.synchronize(dev)
+    if sgqa.sgqa_get_device_error():
+        raise RuntimeError("device error in decode")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    nb = sum((L - 1) // wl.B for L in inp.ctx_len)           # blocks scored per group
+    idx_bytes = wl.G * nb * wl.P * 2
+    gather = wl.G * sum(min(wl.k, (L - 1) // wl.B + 1) for L in inp.ctx_len) * wl.B * wl.D * 2 * 2
+    hbm, _, _, src = load_peaks()
+    return {
+        "metric": "Sparse GQA decode step latency (8 sequences, 256K-1M context)",
+        "value": round(ms, 4), "unit": "ms/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "tokens_per_s": round(batch / (ms / 1e3), 1), "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"decode: {batch} sequences, ctx_len {inp.ctx_len}, G={wl.G} x Hg={wl.Hg}, D={wl.D}, "
+                               f"P={wl.P}, block {wl.B}, top-k {wl.k}",
+                   "l2": "flushed before every step"},
+        "roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + gather + 4 * wl.G * nb * 2,
+                     "roofline_ms": round((idx_bytes + gather + 8 * wl.G * nb) / (hbm * 1e9) * 1e3, 4),
+                     "peak": hbm, "peak_source": src},
+    }
+
+
+# ---------------------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ---------------------------------------------------------------------------------------
 
@@ -471,7 +535,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["sgqa", "reference"], default="sgqa")
-    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "chunk1m", "l128k_tail"])
+    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "chunk1m", "l128k_tail", "decode"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-coverage", action="store_true")
@@ -486,6 +550,10 @@ def main():
         if rank != 0:
             return 0
         print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+    if args.workload == "decode":
+        if rank == 0:
+            print(json.dumps(run_decode(args, local_rank)), flush=True)
         return 0
     if world > 1:
         torch.cuda.set_device(local_rank)
