@@ -387,8 +387,12 @@ def run_sgqa(args, rank, world, local_rank):
     if rank == 0 and not args.no_coverage and wl.q_start == 0 and wl.B == 8:
         coverage = coverage_diagnostic(sgqa, gen, wl, inp, plan, dev)
 
-    n_chunks = math.ceil(wl.T / min(wl.T, 8192))
-    launches_per_step = 1 + 2 * n_chunks + 1
+    # K1 once, K2 + top-k per 8,192-row pass (top-k in two launches for rows past 16,384
+    # candidates: per-slice selection, then the merge), K4 once
+    launches_per_step = 2
+    for r0 in range(0, wl.T, 8192):
+        cand_last = (wl.q_start + min(wl.T, r0 + 8192) - 1) // wl.B
+        launches_per_step += (1 if cand_last > 0 else 0) + (2 if cand_last > 16384 and wl.k > 1 else 1)
     clocks = clk.summary()
     out = {
         "metric": METRIC,

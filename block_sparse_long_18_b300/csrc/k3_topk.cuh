@@ -17,8 +17,13 @@
 // they are ranked in index order and the first `skip` of them are passed over.  The
 // compaction writes the kept indices in ascending order: per group j each warp scans its
 // lanes' counts, one block-wide scan over the (j, warp) totals places the warps.  Rows up to
-// NT*PER candidates keep their keys in registers; longer rows (contexts past 128K tokens at
-// B = 8) are processed in tiles of NT*PER, re-read for every pass.
+// NT*PER candidates keep their keys in registers.  Longer rows (contexts past 128K tokens at
+// B = 8) take two levels: K3_SEGMENT CTAs each select the k-1 best of one NT*PER slice as
+// (key, index) pairs, and a K3_MERGE CTA selects the k-1 best of the concatenated lists.  The
+// result is exact: a candidate with fewer than k-1 candidates ahead of it in the whole row
+// has fewer than k-1 ahead of it in its own slice, and the concatenation keeps index order,
+// so the tie rule carries over.  A STREAM instance (tiles of NT*PER re-read for every pass)
+// serves rows whose merge lists would not fit in registers either.
 #pragma once
 #include "ptx.cuh"
 
@@ -35,7 +40,19 @@ struct K3Args {
   int32_t* sel_idx;     // [G, T_out, k]
   int32_t* sel_cnt;     // [G, T_out]
   int32_t use_pos;      // decode: positions come from pos[]
+  // two-level selection of long rows (more candidates than one CTA holds in registers):
+  uint32_t* pair_key;   // [G * rows, nseg * (k-1)] keys of each segment's local selection
+  int32_t* pair_idx;    // [G * rows, nseg * (k-1)] their candidate indices (ascending per segment)
+  int32_t* pair_cnt;    // [G * rows, nseg] entries each segment kept
+  int32_t nseg;         // segments per row
   int64_t pos[256];     // decode: absolute position of each row's query
+};
+
+// What a k3_topk launch reads and writes.
+enum K3Mode : int {
+  K3_DIRECT = 0,  // candidates = the row's scores; writes the final selection
+  K3_SEGMENT = 1, // candidates = one segment of the row's scores; writes (key, index) pairs
+  K3_MERGE = 2    // candidates = the row's segment pairs; writes the final selection
 };
 
 __device__ __forceinline__ uint32_t score_key(float f) {
@@ -74,7 +91,7 @@ __device__ __forceinline__ uint32_t k3_block_excl_scan(uint32_t v, uint32_t* war
   return before + incl - v;
 }
 
-template <int NT, int PER, bool STREAM>
+template <int NT, int PER, bool STREAM, int MODE = K3_DIRECT>
 __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __grid_constant__ K3Args a) {
   constexpr int NBINS = 2048;
   constexpr int BPT = NBINS / NT;  // bins per thread
@@ -87,28 +104,50 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   __shared__ uint32_t jw_cnt[NJ * NW];  // counts per (group j, warp), then their exclusive scan
   __shared__ uint32_t sh_digit, sh_above, sh_eq;
 
-  const int64_t r = blockIdx.x;
+  constexpr int SEGLEN = NT * PER;  // candidates per segment (K3_SEGMENT)
+  const int64_t r = MODE == K3_SEGMENT ? blockIdx.x / a.nseg : blockIdx.x;  // (group, row) of the launch
+  const int seg = MODE == K3_SEGMENT ? (int)(blockIdx.x % a.nseg) : 0;
   const int64_t g = r / a.rows;
   const int64_t i = r % a.rows;
   const int64_t pos = a.use_pos ? a.pos[i] : a.pos0 + i;
   const int64_t bt = pos / a.B;
-  const int64_t n = bt;  // candidates 0 .. bt-1
   const int need = a.k - 1;
+  const int64_t pstride = (int64_t)a.nseg * need;  // pair slots per row
   int32_t* out = a.sel_idx + ((g * a.T_out) + a.out_row0 + i) * a.k;
   const float* row = a.scores + (g * a.rows + i) * a.ld;
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31, warp = tid >> 5;
-
-  if (n <= need) {  // every causal block is kept
-    for (int64_t j = tid; j < a.k; j += NT) out[j] = j < n ? (int32_t)j : (j == n ? (int32_t)bt : -1);
-    if (tid == 0) a.sel_cnt[g * a.T_out + a.out_row0 + i] = (int32_t)(n + 1);
-    return;
+  // n: candidate slots of this CTA; base: candidate index of slot 0 (K3_SEGMENT)
+  int64_t n = bt, base = 0;
+  if (MODE == K3_SEGMENT) {
+    base = (int64_t)seg * SEGLEN;
+    n = bt - base < SEGLEN ? bt - base : SEGLEN;
+    if (n < 0) n = 0;
+  } else if (MODE == K3_MERGE) {
+    n = pstride;
   }
-  if (need == 0) {  // k = 1: the own block alone
-    if (tid == 0) {
+
+  if (need == 0) {  // k = 1: the own block alone (segmented launches are never made for k = 1)
+    if (MODE != K3_SEGMENT && tid == 0) {
       out[0] = (int32_t)bt;
       a.sel_cnt[g * a.T_out + a.out_row0 + i] = 1;
     }
+    return;
+  }
+  if (MODE == K3_SEGMENT) {
+    uint32_t* pk = a.pair_key + r * pstride + (int64_t)seg * need;
+    int32_t* pi = a.pair_idx + r * pstride + (int64_t)seg * need;
+    if (n <= need) {  // the whole segment is kept; empty slots carry key 0 (below any score)
+      for (int64_t j = tid; j < need; j += NT) {
+        pk[j] = j < n ? score_key(__ldg(row + base + j)) : 0u;
+        pi[j] = j < n ? (int32_t)(base + j) : -1;
+      }
+      if (tid == 0) a.pair_cnt[r * a.nseg + seg] = (int32_t)n;
+      return;
+    }
+  } else if (bt <= need) {  // every causal block is kept
+    for (int64_t j = tid; j < a.k; j += NT) out[j] = j < bt ? (int32_t)j : (j == bt ? (int32_t)bt : -1);
+    if (tid == 0) a.sel_cnt[g * a.T_out + a.out_row0 + i] = (int32_t)(bt + 1);
     return;
   }
 
@@ -116,19 +155,23 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   // candidate index of key e of group j in tile `tile`
   auto kidx = [&](int tile, int j, int e) -> int32_t { return tile * TILE + 4 * (j * NT + tid) + e; };
   uint32_t key[PER];
+  const uint32_t* mkeys = a.pair_key + r * pstride;  // K3_MERGE input (key 0 in unused slots)
   auto load_tile = [&](int tile) {
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       const int32_t b = kidx(tile, j, 0);
-      if (b + 3 < n) {
-        const float4 f = __ldg(reinterpret_cast<const float4*>(row + b));
+      if (MODE == K3_MERGE) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) key[4 * j + e] = (b + e < n) ? __ldg(mkeys + b + e) : 0u;
+      } else if (b + 3 < n && ((base + b) & 3) == 0) {
+        const float4 f = __ldg(reinterpret_cast<const float4*>(row + base + b));
         key[4 * j] = score_key(f.x);
         key[4 * j + 1] = score_key(f.y);
         key[4 * j + 2] = score_key(f.z);
         key[4 * j + 3] = score_key(f.w);
       } else {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) key[4 * j + e] = (b + e < n) ? score_key(__ldg(row + b + e)) : 0u;
+        for (int e = 0; e < 4; ++e) key[4 * j + e] = (b + e < n) ? score_key(__ldg(row + base + b + e)) : 0u;
       }
     }
   };
@@ -136,6 +179,22 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     sh_digit = 0;
     sh_above = 0;
     sh_eq = 0;
+  }
+  if (MODE == K3_MERGE) {
+    // rows whose candidates all fit in k-1 (short rows of a long launch): keep every real entry
+    int64_t real = 0;
+    for (int s2 = 0; s2 < a.nseg; ++s2) real += a.pair_cnt[r * a.nseg + s2];
+    if (real <= need) {
+      if (tid == 0) {
+        int o = 0;
+        for (int64_t j = 0; j < pstride; ++j)
+          if (mkeys[j] != 0u) out[o++] = a.pair_idx[r * pstride + j];
+        out[o] = (int32_t)bt;
+        for (int j = o + 1; j < a.k; ++j) out[j] = -1;
+        a.sel_cnt[g * a.T_out + a.out_row0 + i] = o + 1;
+      }
+      return;
+    }
   }
   if (!STREAM) load_tile(0);
 
@@ -259,13 +318,23 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
       uint32_t o = out_base + (ex >> 16) + (ties_before > skip ? ties_before - skip : 0u) - kept_prev;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int32_t idx = (int32_t)kidx(tile, j, e);
+        const int32_t slot = (int32_t)kidx(tile, j, e);
         const uint32_t kh = key[4 * j + e] & pmask;
-        if (kh > prefix) {
-          out[o++] = idx;
-        } else if (kh == prefix) {
-          if (ties_before >= skip) out[o++] = idx;
+        bool keep = kh > prefix;
+        if (kh == prefix) {
+          keep = ties_before >= skip;
           ++ties_before;
+        }
+        if (keep) {
+          if (MODE == K3_SEGMENT) {
+            a.pair_key[r * pstride + (int64_t)seg * need + o] = key[4 * j + e];
+            a.pair_idx[r * pstride + (int64_t)seg * need + o] = (int32_t)(base + slot);
+          } else if (MODE == K3_MERGE) {
+            out[o] = __ldg(a.pair_idx + r * pstride + slot);
+          } else {
+            out[o] = slot;
+          }
+          ++o;
         }
       }
     }
@@ -275,8 +344,12 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     __syncthreads();  // jw_cnt / warp_tot are rewritten by the next tile
   }
   if (tid == 0) {
-    out[need] = (int32_t)bt;
-    a.sel_cnt[g * a.T_out + a.out_row0 + i] = a.k;
+    if (MODE == K3_SEGMENT) {
+      a.pair_cnt[r * a.nseg + seg] = need;
+    } else {
+      out[need] = (int32_t)bt;
+      a.sel_cnt[g * a.T_out + a.out_row0 + i] = a.k;
+    }
   }
 }
 

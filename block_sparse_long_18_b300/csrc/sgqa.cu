@@ -181,21 +181,67 @@ cudaError_t launch_k2(const K2Args& a, const CUtensorMap& ta, const CUtensorMap&
   return cudaGetLastError();
 }
 
+// Segments per row of the two-level top-k for rows of up to max_cand candidates: 0 when one
+// CTA holds the row in registers (or k = 1), or when the merged lists would not fit either
+// (the streaming instance then serves the row).
+int64_t k3_segments(const Prm& p, int64_t max_cand) {
+  if (max_cand <= kK3RegRow || p.k < 2) return 0;
+  const int64_t nseg = cdiv(max_cand, kK3RegRow);
+  return nseg * (p.k - 1) <= kK3RegRow ? nseg : 0;
+}
+
+// Layout of the top-k workspace for `rows` rows: fp32 scores [G, rows, ld], then (for
+// segmented rows) pair keys and indices [G * rows, nseg * (k-1)] and counts [G * rows, nseg].
+struct IndexWs {
+  int64_t ld, nseg;
+  size_t scores, pair_key, pair_idx, pair_cnt, total;  // byte offsets and size
+};
+IndexWs index_ws_layout(const Prm& p, int64_t rows, int64_t max_cand) {
+  IndexWs w{};
+  w.ld = std::max<int64_t>(4, (int64_t)align_up((size_t)max_cand, 4));
+  w.nseg = k3_segments(p, max_cand);
+  const size_t r = (size_t)p.G * rows;
+  w.scores = 0;
+  w.pair_key = align_up(r * w.ld * 4, 256);
+  w.pair_idx = w.pair_key + align_up(r * w.nseg * (p.k - 1) * 4, 256);
+  w.pair_cnt = w.pair_idx + align_up(r * w.nseg * (p.k - 1) * 4, 256);
+  w.total = w.pair_cnt + align_up(r * w.nseg * 4, 256);
+  return w;
+}
+
 // One CTA per row; the block is the smallest whose registers (32 keys per thread) hold
-// the launch's longest row, so short rows do not pay for empty slots.
-cudaError_t launch_k3(const K3Args& a, int64_t max_cand, cudaStream_t st) {
+// the launch's longest row, so short rows do not pay for empty slots.  Longer rows go
+// through the segment + merge pair when `wsl` gives them pair buffers inside `ws`.
+cudaError_t launch_k3(K3Args a, int64_t max_cand, uint8_t* ws, const IndexWs& wsl, cudaStream_t st) {
   const int64_t grid = (int64_t)a.G * a.rows;
   if (grid <= 0) return cudaSuccess;
-  if (max_cand <= 128 * kK3Per)
+  if (max_cand <= 128 * kK3Per) {
     k3_topk<128, kK3Per, false><<<(unsigned)grid, 128, 0, st>>>(a);
-  else if (max_cand <= 256 * kK3Per)
+  } else if (max_cand <= 256 * kK3Per) {
     k3_topk<256, kK3Per, false><<<(unsigned)grid, 256, 0, st>>>(a);
-  else if (max_cand <= kK3RegRow)
+  } else if (max_cand <= kK3RegRow) {
     k3_topk<kK3Threads, kK3Per, false><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
-  else
+  } else if (wsl.nseg > 0 && cdiv(max_cand, kK3RegRow) <= wsl.nseg) {
+    a.nseg = (int32_t)cdiv(max_cand, kK3RegRow);
+    a.pair_key = reinterpret_cast<uint32_t*>(ws + wsl.pair_key);
+    a.pair_idx = reinterpret_cast<int32_t*>(ws + wsl.pair_idx);
+    a.pair_cnt = reinterpret_cast<int32_t*>(ws + wsl.pair_cnt);
+    k3_topk<kK3Threads, kK3Per, false, K3_SEGMENT><<<(unsigned)(grid * a.nseg), kK3Threads, 0, st>>>(a);
+    const int64_t slots = (int64_t)a.nseg * (a.k - 1);
+    if (slots <= 128 * kK3Per)
+      k3_topk<128, kK3Per, false, K3_MERGE><<<(unsigned)grid, 128, 0, st>>>(a);
+    else if (slots <= 256 * kK3Per)
+      k3_topk<256, kK3Per, false, K3_MERGE><<<(unsigned)grid, 256, 0, st>>>(a);
+    else
+      k3_topk<kK3Threads, kK3Per, false, K3_MERGE><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
+  } else {
     k3_topk<kK3Threads, kK3Per, true><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
+  }
   return cudaGetLastError();
 }
+
+// Kernel launches of one top-k call over rows of up to max_cand candidates.
+int k3_launches(const Prm& p, int64_t max_cand) { return k3_segments(p, max_cand) > 0 ? 2 : 1; }
 
 cudaError_t launch_k1(const K1Args& a, cudaStream_t st) {
   const int64_t n_vec = (int64_t)a.G * a.n_blocks * (a.P / 8);
@@ -205,28 +251,29 @@ cudaError_t launch_k1(const K1Args& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// Bytes of the indexer score workspace for `rows` query rows whose largest candidate count
-// is max_cand.
-size_t index_ws_bytes(const Prm& p, int64_t rows, int64_t max_cand) {
-  const int64_t ld = std::max<int64_t>(4, align_up((size_t)max_cand, 4));
-  return align_up((size_t)p.G * rows * ld * 4, 256);
-}
+// Bytes of the indexer + top-k workspace for `rows` query rows whose largest candidate
+// count is max_cand.
+size_t index_ws_bytes(const Prm& p, int64_t rows, int64_t max_cand) { return index_ws_layout(p, rows, max_cand).total; }
 
 // ---- the indexer + top-k over rows [0, T) at positions q_start .. ----
 sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t q_start, const void* k_blk,
                            int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes,
                            cudaStream_t st) {
   const int64_t max_cand = (q_start + T - 1) / p.B;  // candidates of the last row
-  const int64_t ld = std::max<int64_t>(4, (int64_t)align_up((size_t)max_cand, 4));
   // rows per pass: as many as the workspace holds, preferring kIndexChunkRows
   int64_t rows = std::min<int64_t>(T, kIndexChunkRows);
-  const size_t per_row = (size_t)p.G * ld * 4;
-  const int64_t fit = (int64_t)(ws_bytes / per_row);
-  if (fit < rows) {
-    rows = fit >= 128 ? fit / 128 * 128 : fit;
+  if (index_ws_bytes(p, rows, max_cand) > ws_bytes) {
+    int64_t lo = 0, hi = rows;  // largest row count that fits
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) / 2;
+      if (index_ws_bytes(p, mid, max_cand) <= ws_bytes) lo = mid; else hi = mid - 1;
+    }
+    rows = lo >= 128 ? lo / 128 * 128 : lo;
     if (rows < std::min<int64_t>(T, 128)) return SGQA_ERR_WORKSPACE_TOO_SMALL;
   }
   if (!aligned16(ws)) return SGQA_ERR_INVALID_ARGUMENT;
+  const IndexWs wsl = index_ws_layout(p, rows, max_cand);
+  const int64_t ld = wsl.ld;
   float* scores = static_cast<float*>(ws);
 
   CUtensorMap ta, tb;
@@ -274,7 +321,7 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
     a3.sel_idx = sel_idx;
     a3.sel_cnt = sel_cnt;
     a3.use_pos = 0;
-    SGQA_CUDA_OK(launch_k3(a3, cand_last, st));
+    SGQA_CUDA_OK(launch_k3(a3, cand_last, static_cast<uint8_t*>(ws), wsl, st));
   }
   return SGQA_OK;
 }
@@ -587,10 +634,11 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
     return SGQA_ERR_INVALID_ARGUMENT;
   const int64_t nb_total = total / p.B;
   const int64_t max_cand = (max_len - 1) / p.B;
-  const int64_t ld = std::max<int64_t>(4, (int64_t)align_up((size_t)max_cand, 4));
+  const IndexWs wsl = index_ws_layout(p, batch, max_cand);
+  const int64_t ld = wsl.ld;
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(w);
-  w += index_ws_bytes(p, batch, max_cand);
+  w += wsl.total;
   const int nsplit = 32;
   float* part_o = reinterpret_cast<float*>(w);
   w += align_up((size_t)p.G * batch * nsplit * 16 * 192 * 4, 256);
@@ -652,7 +700,7 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
     a3.sel_cnt = sel_cnt;
     a3.use_pos = 1;
     for (int i = 0; i < batch; ++i) a3.pos[i] = ctx_len[i] - 1;
-    SGQA_CUDA_OK(launch_k3(a3, max_cand, st));
+    SGQA_CUDA_OK(launch_k3(a3, max_cand, static_cast<uint8_t*>(ws), wsl, st));
   }
   // 4. split-K attention + combine
   {

@@ -101,6 +101,27 @@ SMALL = [
 ]
 
 
+# Rows with more candidates than one top-k CTA holds in registers (16,384): the two-level
+# selection (per-slice lists, then a merge), and the streaming instance where the merged
+# lists would not fit either.  Integer proxies in [-4, 4] over P = 64 give many equal
+# scores, so the tie rule is exercised across slice boundaries.
+LONG_ROWS = [
+    dict(T=96, G=2, Hg=1, B=1, k=33, P=64, q_start=40000),    # 3 slices, merge in 128 threads
+    dict(T=40, G=1, Hg=2, B=1, k=3000, P=64, q_start=36000),  # 3 slices, merge in 512 threads
+    dict(T=24, G=1, Hg=1, B=1, k=6000, P=64, q_start=40000),  # merged lists too long: streaming
+    dict(T=70, G=1, Hg=4, B=1, k=12, P=64, q_start=16350),    # rows on both sides of 16,384
+]
+
+
+@pytest.mark.parametrize("case", LONG_ROWS, ids=[f"q{c['q_start']}_k{c['k']}" for c in LONG_ROWS])
+def test_prefill_long_rows_all_rows(sg, case):
+    wl = gen.small_workload(**case)
+    inp = _to_cuda(gen.make_inputs(wl, seed=4))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    _check_prefill(inp, wl, res, np.arange(wl.T))
+
+
 @pytest.mark.parametrize("case", SMALL, ids=[f"T{c['T']}_B{c['B']}_k{c['k']}_G{c['G']}" for c in SMALL])
 def test_prefill_small_all_rows(sg, case):
     wl = gen.small_workload(**case)
