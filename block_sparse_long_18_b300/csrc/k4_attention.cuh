@@ -60,15 +60,24 @@ struct K4Args {
   int64_t kv_off[256];
 };
 
-// byte offset, inside a 16-key tile, of 16-byte unit u (0..23) of key n (0..15)
+// Byte offset, inside a 16-row tile staged for ldmatrix (Q, gate, output), of 16-byte unit
+// u (0..23) of row n (0..15): row n's 384 bytes are 128-byte lines 3n .. 3n+2, swizzled.
 __device__ __forceinline__ uint32_t k4_off(uint32_t n, uint32_t u) {
   const uint32_t r = n * 3 + (u >> 3);
   return r * 128 + (((u & 7) ^ (r & 7)) << 4);
 }
 
-// PIPE: issue the next stage's Q K^T before this stage's softmax and P V (needs a stage
-// of prefetch beyond the two in use, so it pays only with NSTAGE >= 3).
-template <int NW, int NSTAGE, bool TMA, bool PIPE>
+// Byte offset, inside a stage's K (or V) tile of 16 keys, of 16-byte unit u (0..23) of key
+// n (0..15).  Keys come in two groups of 8; a group holds its three 64-wide chunks of D as
+// 1 KB atoms [chunk][key][64] with the 128-byte swizzle (unit XOR key), which is what one
+// TMA copy of box {64, 8, 3} through a {64, tokens, 3} map with strides {384 B, 128 B}
+// writes.  The swizzle term depends on the key alone, so a lane's ldmatrix addresses are
+// a few per-lane bases plus immediates.
+__device__ __forceinline__ uint32_t k4_kv_off(uint32_t n, uint32_t u) {
+  return (n >> 3) * 3072 + (u >> 3) * 1024 + (n & 7) * 128 + (((u & 7) ^ (n & 7)) << 4);
+}
+
+template <int NW, int NSTAGE, bool TMA>
 __global__ void __launch_bounds__(NW * 32, 1)
     k4_sparse_attn(const __grid_constant__ K4Args a, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV) {
@@ -88,23 +97,34 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int64_t i = gr % a.rows;
   const int64_t t = a.use_pos ? a.pos[i] : a.pos0 + i;
   const int64_t kvo = a.use_pos ? a.kv_off[i] : 0;
-  const int64_t bt = t / a.B;
+  const int32_t bt = (int32_t)(t / a.B);
   const int32_t* sel = a.sel_idx + (g * a.rows + i) * (int64_t)a.kcap;
-  int64_t cnt = a.dense ? bt + 1 : (int64_t)a.sel_cnt[g * a.rows + i];
-  if (cnt < 1 || cnt > (a.dense ? bt + 1 : (int64_t)a.kcap)) {
+  int32_t cnt = a.dense ? bt + 1 : a.sel_cnt[g * a.rows + i];
+  if (cnt < 1 || cnt > (a.dense ? bt + 1 : a.kcap)) {
     report_error(kErrBounds);
     cnt = cnt < 1 ? 1 : (a.dense ? bt + 1 : a.kcap);
   }
-  const int bps = 16 / a.B;  // blocks per stage
-  const int64_t n_st = (cnt + bps - 1) / bps;
-  const int64_t per_split = (n_st + a.nsplit - 1) / a.nsplit;
-  const int64_t s_begin = (int64_t)split * per_split;
-  const int64_t s_end = s_begin + per_split < n_st ? s_begin + per_split : n_st;
+  const int bps = 16 / a.B;  // blocks per stage (B <= 16); a block of 16 is one stage
+  const int32_t n_st = (cnt + bps - 1) / bps;
+  const int32_t per_split = (n_st + a.nsplit - 1) / a.nsplit;
+  const int32_t s_begin = split * per_split;
+  const int32_t s_end = s_begin + per_split < n_st ? s_begin + per_split : n_st;
+  const int64_t row_base = (int64_t)g * a.ctx_cap + kvo;  // cache row of token 0 of this unit
 
-  auto block_of = [&](int64_t j) -> int64_t {  // j-th selected block, or -1 if unused/invalid
+  // Block j of the selection: -1 past the count, -2 for an index outside 0..bt.  The
+  // selection is read 32 entries at a time into a register (`cur` for chunk ccur, `nxt`
+  // for the chunk after it, loaded a chunk ahead) and handed out by shuffles.
+  auto load_chunk = [&](int32_t c) -> int32_t {
+    const int32_t j = c * 32 + (int32_t)lane;
     if (j >= cnt) return -1;
-    const int64_t b = a.dense ? j : (int64_t)__ldg(sel + j);
-    return (b >= 0 && b <= bt) ? b : -2;
+    return a.dense ? j : __ldg(sel + j);
+  };
+  int32_t ccur = (s_begin * bps) >> 5;
+  int32_t cur = load_chunk(ccur), nxt = load_chunk(ccur + 1);
+  auto blk = [&](int32_t j) -> int32_t {  // every lane calls it with the same j
+    const int32_t v = __shfl_sync(0xffffffffu, (j >> 5) == ccur ? cur : nxt, j & 31);
+    if (j >= cnt) return -1;
+    return (v >= 0 && v <= bt) ? v : -2;
   };
 
   // ---- Q fragments: Q[i, g*Hg + h, :] staged swizzled in slot 0, then ldmatrix ----
@@ -139,32 +159,47 @@ __global__ void __launch_bounds__(NW * 32, 1)
   fence_proxy_async_smem();
   __syncwarp();
 
-  // ---- stage loader ----
-  auto issue = [&](int64_t s) {
-    const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
+  // per-lane ldmatrix bases (see k4_kv_off): K as the B operand of S = Q K^T reads key
+  // nt*8 + (lane&7), unit 2kp + (lane>>3); V (transposed) reads key (lane>>3 & 1)*8 +
+  // (lane&7), unit 2dp + (lane>>4).
+  const uint32_t kr = lane & 7;
+  const uint32_t k_lo = kr * 128 + (((lane >> 3) ^ kr) << 4);  // units with (u & 7) < 4
+  const uint32_t k_hi = k_lo ^ 64u;                             // units with (u & 7) >= 4
+  uint32_t v_off[4];
+#pragma unroll
+  for (int jx = 0; jx < 4; ++jx)
+    v_off[jx] = ((lane >> 3) & 1) * 3072 + kr * 128 + (((((lane >> 4) ^ kr)) ^ (2u * jx)) << 4);
+
+  // ---- stage loader (every lane calls it) ----
+  auto issue = [&](int32_t s) {
+    const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
     const uint32_t ks_addr = wbase + slot * K4_STAGE;
     const uint32_t vs_addr = ks_addr + K4_TILE;
     if (TMA) {
+      // B = 8: two blocks of 8 keys; B = 16: the two halves of one block
+      int32_t b0 = blk(s * bps), b1 = bps == 2 ? blk(s * bps + 1) : b0;
+      if (b0 < 0) b0 = bt;  // unused / invalid slot: fetch the own block, masked below
+      if (b1 < 0) b1 = bt;
       if (lane == 0) {
         const uint32_t bar = bar0 + 8 * slot;
         mbar_arrive_expect_tx(bar, K4_STAGE);
-        for (int bi = 0; bi < bps; ++bi) {
-          int64_t b = block_of(s * bps + bi);
-          if (b < 0) b = bt;  // unused / invalid slot: fetch the own block, masked below
-          const int32_t row = (int32_t)((int64_t)g * a.ctx_cap + kvo + b * a.B);
-          tma_load_3d(ks_addr + bi * a.B * 384, &tmK, bar, 0, 0, row);
-          tma_load_3d(vs_addr + bi * a.B * 384, &tmV, bar, 0, 0, row);
-        }
+        const int32_t r0 = (int32_t)(row_base + (int64_t)b0 * a.B);
+        const int32_t r1 = bps == 2 ? (int32_t)(row_base + (int64_t)b1 * a.B) : r0 + 8;
+        tma_load_3d(ks_addr, &tmK, bar, 0, r0, 0);
+        tma_load_3d(ks_addr + 3072, &tmK, bar, 0, r1, 0);
+        tma_load_3d(vs_addr, &tmV, bar, 0, r0, 0);
+        tma_load_3d(vs_addr + 3072, &tmV, bar, 0, r1, 0);
       }
     } else {
       const int64_t row_lim = (int64_t)a.G * a.ctx_cap - 1;
       for (int w = lane; w < 16 * K4_UNITS; w += 32) {
         const uint32_t n = w / K4_UNITS, u = w % K4_UNITS;
-        int64_t b = block_of(s * bps + n / a.B);
-        if (b < 0) b = bt;
-        int64_t row = (int64_t)g * a.ctx_cap + kvo + b * a.B + (n % a.B);
+        const int32_t j = s * bps + (int32_t)n / a.B;
+        int64_t b = j < cnt ? (a.dense ? j : __ldg(sel + j)) : -1;
+        if (b < 0 || b > bt) b = bt;
+        int64_t row = row_base + b * a.B + (n % a.B);
         if (row > row_lim) row = row_lim;
-        const uint32_t off = k4_off(n, u);
+        const uint32_t off = k4_kv_off(n, u);
         cp_async_16(ks_addr + off, a.kc + row * K4_D + u * 8);
         cp_async_16(vs_addr + off, a.vc + row * K4_D + u * 8);
       }
@@ -181,75 +216,76 @@ __global__ void __launch_bounds__(NW * 32, 1)
   constexpr float kLazy = 8.f;
   const uint32_t qd = lane & 3;  // column pair within an 8-wide tile
   bool ok = true;
-  int64_t issued = s_begin;
+  int32_t issued = s_begin;
 
-  auto stage_addr = [&](int64_t s) { return wbase + (uint32_t)((s - s_begin) % NSTAGE) * K4_STAGE; };
-  auto wait_stage = [&](int64_t s) -> bool {
+  auto wait_stage = [&](int32_t s) -> bool {
     if (TMA) {
-      const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
-      return mbar_wait(bar0 + 8 * slot, (uint32_t)(((s - s_begin) / NSTAGE) & 1), a.wait_ns);
+      const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
+      return mbar_wait(bar0 + 8 * slot, (uint32_t)((s - s_begin) / NSTAGE) & 1u, a.wait_ns);
     }
-    if (PIPE) cp_async_wait<NSTAGE - 2>();  // every group but the newest NSTAGE-2 has landed
-    else cp_async_wait<NSTAGE - 1>();
+    cp_async_wait<NSTAGE - 1>();
     __syncwarp();
     return true;
-  };
-  // S = Q K^T for one stage: two n-tiles x 12 k-steps, as four independent chains.
-  auto qk = [&](uint32_t ks_addr, float (&sc)[2][4]) {
-    float acc[2][2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.f;
-#pragma unroll
-    for (int kp = 0; kp < 12; kp += 2) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(ks_addr + k4_off(nt * 8 + (lane & 7), 2 * kp + (lane >> 3)), b0, b1, b2, b3);
-        mma_bf16_16816(acc[nt][0], qa[kp], b0, b1);
-        mma_bf16_16816(acc[nt][1], qa[kp + 1], b2, b3);
-      }
-    }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) sc[nt][e] = acc[nt][0][e] + acc[nt][1][e];
   };
 
   for (int s = 0; s < NSTAGE - 1; ++s)
     if (s_begin + s < s_end) { issue(s_begin + s); issued = s_begin + s + 1; }
     else if (!TMA) cp_async_commit();
 
-  float sc[2][4];
-  if (PIPE && s_begin < s_end) {
-    if (wait_stage(s_begin)) qk(stage_addr(s_begin), sc);
-    else ok = false;
-  }
-
-  for (int64_t s = s_begin; ok && s < s_end; ++s) {
+  for (int32_t s = s_begin; s < s_end; ++s) {
+    // move the selection registers along once this stage's blocks leave chunk ccur
+    if (((s * bps) >> 5) != ccur) {
+      ++ccur;
+      cur = nxt;
+      nxt = load_chunk(ccur + 1);
+    }
     // prefetch into the slot stage s-1 has released
     if (s + NSTAGE - 1 < s_end) { issue(s + NSTAGE - 1); issued = s + NSTAGE; }
     else if (!TMA) cp_async_commit();
-    // scores of the next stage are issued first so their MMAs overlap this stage's softmax
-    float sn[2][4];
-    const bool has_next = PIPE && s + 1 < s_end;
-    if (PIPE) {
-      if (has_next) {
-        if (!wait_stage(s + 1)) { ok = false; break; }
-        qk(stage_addr(s + 1), sn);
-      }
+    // blocks of this stage and whether all are valid and strictly before the own block
+    int32_t cb0 = 0, cb1 = 0;
+    bool fast = true;
+    if (TMA) {
+      cb0 = blk(s * bps);
+      cb1 = bps == 2 ? blk(s * bps + 1) : cb0;
+      fast = cb0 >= 0 && cb0 < bt && cb1 >= 0 && cb1 < bt;
     } else {
-      if (!wait_stage(s)) { ok = false; break; }
-      qk(stage_addr(s), sc);
+      for (int bi = 0; bi < bps; ++bi) {
+        const int32_t j = s * bps + bi;
+        const int32_t b = j < cnt ? (a.dense ? j : __ldg(sel + j)) : -1;
+        fast = fast && b >= 0 && b < bt;
+      }
+    }
+    if (!wait_stage(s)) { ok = false; break; }
+    const uint32_t ks_addr = wbase + ((uint32_t)(s - s_begin) % NSTAGE) * K4_STAGE;
+    const uint32_t vs_addr = ks_addr + K4_TILE;
+
+    // ---- S = Q K^T: two n-tiles x 12 k-steps as four independent chains ----
+    float sc[2][4];
+    {
+      float acc[2][2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) acc[nt][h][0] = acc[nt][h][1] = acc[nt][h][2] = acc[nt][h][3] = 0.f;
+      const uint32_t klo = ks_addr + k_lo, khi = ks_addr + k_hi;
+#pragma unroll
+      for (int kp = 0; kp < 12; kp += 2) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(((kp & 2) ? khi : klo) + nt * 3072 + (kp >> 2) * 1024, b0, b1, b2, b3);
+          mma_bf16_16816(acc[nt][0], qa[kp], b0, b1);
+          mma_bf16_16816(acc[nt][1], qa[kp + 1], b2, b3);
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] = acc[nt][0][e] + acc[nt][1][e];
     }
 
     // ---- scale; mask unused slots, invalid indices and tokens after t ----
-    bool fast = true;  // every block of the stage valid and strictly before the own block
-    for (int bi = 0; bi < bps; ++bi) {
-      const int64_t b = block_of(s * bps + bi);
-      fast = fast && b >= 0 && b < bt;
-    }
     if (fast) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -261,8 +297,15 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           const int key = nt * 8 + 2 * qd + c;
-          const int64_t b = block_of(s * bps + key / a.B);
-          const bool valid = b >= 0 && b * a.B + (key % a.B) <= t;
+          int32_t b;
+          if (TMA) {
+            b = (nt == 1 && bps == 2) ? cb1 : cb0;
+          } else {
+            const int32_t j = s * bps + key / a.B;
+            const int32_t raw = j < cnt ? (a.dense ? j : __ldg(sel + j)) : -1;
+            b = j >= cnt ? -1 : ((raw >= 0 && raw <= bt) ? raw : -2);
+          }
+          const bool valid = b >= 0 && (int64_t)b * a.B + (key % a.B) <= t;
           if (b == -2) report_error(kErrBounds);
           sc[nt][c] = valid ? sc[nt][c] * a.scale_log2 : -INFINITY;
           sc[nt][2 + c] = valid ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
@@ -274,8 +317,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
     float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
@@ -311,30 +354,22 @@ __global__ void __launch_bounds__(NW * 32, 1)
     pa[3] = pack_bf16(p[1][2], p[1][3]);
 
     // ---- O += P V ----
-    const uint32_t vs_addr = stage_addr(s) + K4_TILE;
 #pragma unroll
     for (int dp = 0; dp < 12; ++dp) {
-      const uint32_t mtx = lane >> 3;
       uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vs_addr + k4_off((mtx & 1) * 8 + (lane & 7), 2 * dp + (mtx >> 1)), v0, v1, v2, v3);
+      ldsm_x4_t(vs_addr + v_off[dp & 3] + (dp >> 2) * 1024, v0, v1, v2, v3);
       mma_bf16_16816(o[2 * dp], pa, v0, v1);
       mma_bf16_16816(o[2 * dp + 1], pa, v2, v3);
     }
     __syncwarp();  // every lane is done with this stage's slot
-    if (has_next) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] = sn[nt][e];
-    }
   }
 
   if (!ok) {
     // drain the copies still in flight into this warp's slots, then leave
     if (TMA && lane == 0) {
-      for (int64_t s = issued - NSTAGE > s_begin ? issued - NSTAGE : s_begin; s < issued; ++s) {
-        const uint32_t slot = (uint32_t)((s - s_begin) % NSTAGE);
-        mbar_wait(bar0 + 8 * slot, (uint32_t)(((s - s_begin) / NSTAGE) & 1), kDrainLimitNs);
+      for (int32_t s = issued - NSTAGE > s_begin ? issued - NSTAGE : s_begin; s < issued; ++s) {
+        const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
+        mbar_wait(bar0 + 8 * slot, (uint32_t)((s - s_begin) / NSTAGE) & 1u, kDrainLimitNs);
       }
     }
     __syncwarp();

@@ -112,22 +112,17 @@ int num_sms() {
   return n;
 }
 
-// ---- attention launch configuration (warps per CTA, stages per warp, pipelined QK) ----
+// ---- attention launch configuration (warps per CTA x stages per warp) ----
 struct K4Cfg {
-  int nw, ns, pipe;
+  int nw, ns;
 };
 K4Cfg k4_cfg() {
   static K4Cfg c = [] {
-    K4Cfg d{8, 2, 0};
+    K4Cfg d{8, 2};
     if (const char* e = std::getenv("SGQA_K4_CFG")) {
       int a = 0, b = 0;
-      char pc = 0;
-      const int n = std::sscanf(e, "%dx%d%c", &a, &b, &pc);
-      if (n >= 2) {
-        const int pipe = (n == 3 && pc == 'p') ? 1 : 0;
-        const bool known = (a == 8 && b == 2) || (a == 6 && b == 3) || (a == 4 && b == 4) || (a == 5 && b == 3);
-        if (known) d = K4Cfg{a, b, pipe};
-      }
+      if (std::sscanf(e, "%dx%d", &a, &b) == 2 && ((a == 8 && b == 2) || (a == 6 && b == 3) || (a == 4 && b == 4)))
+        d = K4Cfg{a, b};
     }
     return d;
   }();
@@ -136,34 +131,35 @@ K4Cfg k4_cfg() {
 
 size_t k4_smem(int nw, int ns) { return (size_t)nw * ns * K4_STAGE + (size_t)nw * ns * 8 + 1024; }
 
-template <int NW, int NS, bool TMA, bool PIPE>
+template <int NW, int NS, bool TMA>
 cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
                         cudaStream_t st) {
   const size_t smem = k4_smem(NW, NS);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k4_sparse_attn<NW, NS, TMA, PIPE>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k4_sparse_attn<NW, NS, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
   const int64_t grid = cdiv(n_units, NW);
-  k4_sparse_attn<NW, NS, TMA, PIPE><<<(unsigned)grid, NW * 32, smem, st>>>(a, tk, tv);
+  k4_sparse_attn<NW, NS, TMA><<<(unsigned)grid, NW * 32, smem, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_k4(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units, bool tma,
                       cudaStream_t st) {
-  if (!tma) return launch_k4_t<8, 2, false, false>(a, tk, tv, n_units, st);
+  if (!tma) return launch_k4_t<8, 2, false>(a, tk, tv, n_units, st);
   const K4Cfg c = k4_cfg();
-  if (c.nw == 6 && c.ns == 3) return c.pipe ? launch_k4_t<6, 3, true, true>(a, tk, tv, n_units, st)
-                                            : launch_k4_t<6, 3, true, false>(a, tk, tv, n_units, st);
-  if (c.nw == 5 && c.ns == 3) return c.pipe ? launch_k4_t<5, 3, true, true>(a, tk, tv, n_units, st)
-                                            : launch_k4_t<5, 3, true, false>(a, tk, tv, n_units, st);
-  if (c.nw == 4 && c.ns == 4) return c.pipe ? launch_k4_t<4, 4, true, true>(a, tk, tv, n_units, st)
-                                            : launch_k4_t<4, 4, true, false>(a, tk, tv, n_units, st);
-  return c.pipe ? launch_k4_t<8, 2, true, true>(a, tk, tv, n_units, st)
-                : launch_k4_t<8, 2, true, false>(a, tk, tv, n_units, st);
+  if (c.nw == 6) return launch_k4_t<6, 3, true>(a, tk, tv, n_units, st);
+  if (c.nw == 4) return launch_k4_t<4, 4, true>(a, tk, tv, n_units, st);
+  return launch_k4_t<8, 2, true>(a, tk, tv, n_units, st);
+}
+
+// K and V cache maps for the attention kernels: dims {64, tokens, 3 chunks} with strides
+// {384 B, 128 B}; one copy of box {64, 8, 3} lands 8 tokens as three 1 KB swizzle atoms.
+bool make_kv_map(CUtensorMap* m, const void* base, uint64_t tokens) {
+  return make_map_3d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 64, tokens, 3, 384, 128, 64, 8, 3);
 }
 
 cudaError_t launch_k2(const K2Args& a, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
@@ -239,9 +235,6 @@ cudaError_t launch_k3(K3Args a, int64_t max_cand, uint8_t* ws, const IndexWs& ws
   }
   return cudaGetLastError();
 }
-
-// Kernel launches of one top-k call over rows of up to max_cand candidates.
-int k3_launches(const Prm& p, int64_t max_cand) { return k3_segments(p, max_cand) > 0 ? 2 : 1; }
 
 cudaError_t launch_k1(const K1Args& a, cudaStream_t st) {
   const int64_t n_vec = (int64_t)a.G * a.n_blocks * (a.P / 8);
@@ -383,10 +376,7 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
     const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
     if (!make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 64, 3, (uint64_t)T * p.H, 128, 384, 64, 1, 16))
       return SGQA_ERR_CUDA;
-    // Block-major maps: dims {64, tokens, 3 chunks} with strides {384 B, 128 B}, so one copy
-    // of box {64, 8, 3} lands a block as its three 1 KB atoms.
-    if (!make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, 64, rowsz, 3, 384, 128, 64, 8, 3)) return SGQA_ERR_CUDA;
-    if (!make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, 64, rowsz, 3, 384, 128, 64, 8, 3)) return SGQA_ERR_CUDA;
+    if (!make_kv_map(&tk, k, rowsz) || !make_kv_map(&tv, v, rowsz)) return SGQA_ERR_CUDA;
     a.block_major = 1;
     SGQA_CUDA_OK(launch_k4tc(a, tq, tk, tv, st));
     return SGQA_OK;
@@ -418,8 +408,7 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
   CUtensorMap tk{}, tv{};
   if (tma) {
     const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
-    if (!make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, 64, 3, rowsz, 128, 384, 64, 3, p.B)) return SGQA_ERR_CUDA;
-    if (!make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, 64, 3, rowsz, 128, 384, 64, 3, p.B)) return SGQA_ERR_CUDA;
+    if (!make_kv_map(&tk, k, rowsz) || !make_kv_map(&tv, v, rowsz)) return SGQA_ERR_CUDA;
   }
   SGQA_CUDA_OK(launch_k4(a, tk, tv, (int64_t)p.G * T, tma, st));
   return SGQA_OK;
@@ -737,10 +726,7 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
     CUtensorMap tk{}, tv{};
     if (tma) {
       const uint64_t rowsz = (uint64_t)p.G * total;
-      if (!make_map_3d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, 64, 3, rowsz, 128, 384, 64, 3, p.B))
-        return SGQA_ERR_CUDA;
-      if (!make_map_3d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, 64, 3, rowsz, 128, 384, 64, 3, p.B))
-        return SGQA_ERR_CUDA;
+      if (!make_kv_map(&tk, k_cache, rowsz) || !make_kv_map(&tv, v_cache, rowsz)) return SGQA_ERR_CUDA;
     }
     SGQA_CUDA_OK(launch_k4(a, tk, tv, (int64_t)p.G * batch * nsplit, tma, st));
     K4CombineArgs c{};
