@@ -10,15 +10,18 @@
 //
 // One warp owns one (row, group) unit: its 16 heads are the M = 16 of mma.sync m16n8k16
 // (bf16 in, fp32 accumulate), so every gathered K/V byte serves all 16 heads.  The warp
-// walks its selection 16 keys per stage (two blocks of 8).  Each block of a group is one
-// contiguous 8 x 192 bf16 run in the group-major cache, fetched by ONE TMA copy per
-// tensor through a 3-D tensor map {64, 3, tokens} with 128-byte swizzle; the smem row of
-// (token n, 64-wide chunk c) is 3n + c, and since 3 is odd, ldmatrix over 8 consecutive
-// tokens of one chunk touches 8 distinct 16-byte bank groups.  Stages cycle through a
-// per-warp ring of mbarriers (bounded waits).  S = Q K^T (2 n-tiles x 12 k-steps), online
-// softmax in fp32 (exp2 domain, masked keys -inf), P goes straight from the accumulator
-// layout into the A operand of P V (24 n-tiles over D).  The epilogue normalises, applies
-// sigmoid(gate) and writes bf16 through a swizzled smem tile with 16-byte stores.
+// walks its selection 16 keys per stage (two blocks of 8, or one of 16), two stages per
+// warp: one in flight while the other is consumed.  Every 8 keys of a tensor arrive by ONE
+// TMA copy of box {64, 8, 3} through a {64, tokens, 3} tensor map whose strides are
+// {384 B, 128 B}: it lands the keys as three 1 KB atoms [chunk][key][64] with the 128-byte
+// swizzle, whose XOR term is the key alone, so the ldmatrix addresses of a stage are six
+// per-lane bases plus immediates.  The selection is read 32 entries at a time into a
+// register and handed out by shuffles.  S = Q K^T (2 n-tiles x 12 k-steps), online
+// softmax in fp32 (exp2 domain, masked keys -inf, reference maxima refreshed lazily), P
+// goes straight from the accumulator layout into the A operand of P V (24 n-tiles over
+// D).  The epilogue normalises, applies sigmoid(gate) and writes bf16 through a swizzled
+// smem tile with 16-byte stores.  Blocks smaller than 8 are gathered with cp.async into
+// the same layout.
 //
 // Units are numbered group-major, so the CTAs in flight at any moment gather from one
 // group's K/V (100 MB at 128K tokens), which the 126 MB L2 can hold.
@@ -77,10 +80,11 @@ __device__ __forceinline__ uint32_t k4_kv_off(uint32_t n, uint32_t u) {
   return (n >> 3) * 3072 + (u >> 3) * 1024 + (n & 7) * 128 + (((u & 7) ^ (n & 7)) << 4);
 }
 
-template <int NW, int NSTAGE, bool TMA>
+template <int NW, bool TMA>
 __global__ void __launch_bounds__(NW * 32, 1)
     k4_sparse_attn(const __grid_constant__ K4Args a, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV) {
+  constexpr int NSTAGE = 2;  // a stage in flight while the other is consumed
   extern __shared__ uint8_t k4_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(k4_smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t warp = threadIdx.x >> 5;
@@ -170,7 +174,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
   for (int jx = 0; jx < 4; ++jx)
     v_off[jx] = ((lane >> 3) & 1) * 3072 + kr * 128 + (((((lane >> 4) ^ kr)) ^ (2u * jx)) << 4);
 
-  // ---- stage loader (every lane calls it) ----
+  // ---- stage loader (every lane calls it); nb0/nb1 keep the blocks of the stage issued
+  // last, which the next iteration masks with ----
+  int32_t nb0 = 0, nb1 = 0;
   auto issue = [&](int32_t s) {
     const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
     const uint32_t ks_addr = wbase + slot * K4_STAGE;
@@ -178,6 +184,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if (TMA) {
       // B = 8: two blocks of 8 keys; B = 16: the two halves of one block
       int32_t b0 = blk(s * bps), b1 = bps == 2 ? blk(s * bps + 1) : b0;
+      nb0 = b0;
+      nb1 = b1;
       if (b0 < 0) b0 = bt;  // unused / invalid slot: fetch the own block, masked below
       if (b1 < 0) b1 = bt;
       if (lane == 0) {
@@ -239,15 +247,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
       cur = nxt;
       nxt = load_chunk(ccur + 1);
     }
+    // blocks of this stage (fetched by the previous issue) and whether all are valid and
+    // strictly before the own block
+    const int32_t cb0 = nb0, cb1 = nb1;
     // prefetch into the slot stage s-1 has released
     if (s + NSTAGE - 1 < s_end) { issue(s + NSTAGE - 1); issued = s + NSTAGE; }
     else if (!TMA) cp_async_commit();
-    // blocks of this stage and whether all are valid and strictly before the own block
-    int32_t cb0 = 0, cb1 = 0;
     bool fast = true;
     if (TMA) {
-      cb0 = blk(s * bps);
-      cb1 = bps == 2 ? blk(s * bps + 1) : cb0;
       fast = cb0 >= 0 && cb0 < bt && cb1 >= 0 && cb1 < bt;
     } else {
       for (int bi = 0; bi < bps; ++bi) {
@@ -285,13 +292,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
         for (int e = 0; e < 4; ++e) sc[nt][e] = acc[nt][0][e] + acc[nt][1][e];
     }
 
-    // ---- scale; mask unused slots, invalid indices and tokens after t ----
-    if (fast) {
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] *= a.scale_log2;
-    } else {
+    // ---- mask unused slots, invalid indices and tokens after t (scores stay unscaled) ----
+    if (!fast) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
@@ -307,20 +309,25 @@ __global__ void __launch_bounds__(NW * 32, 1)
           }
           const bool valid = b >= 0 && (int64_t)b * a.B + (key % a.B) <= t;
           if (b == -2) report_error(kErrBounds);
-          sc[nt][c] = valid ? sc[nt][c] * a.scale_log2 : -INFINITY;
-          sc[nt][2 + c] = valid ? sc[nt][2 + c] * a.scale_log2 : -INFINITY;
+          if (!valid) {
+            sc[nt][c] = -INFINITY;
+            sc[nt][2 + c] = -INFINITY;
+          }
         }
       }
     }
 
-    // ---- online softmax, rows r = lane/4 and r + 8 ----
-    float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-    float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    // ---- online softmax (log2 domain), rows r = lane/4 and r + 8 ----
+    // A row's quad shares its reference maximum; the quad maximum is needed only when some
+    // lane's own scores pass the reference by more than kLazy, which one vote detects.
+    const float sl2 = a.scale_log2;
+    float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1])) * sl2;
+    float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3])) * sl2;
     if (__any_sync(0xffffffffu, mx0 > m0 + kLazy || mx1 > m1 + kLazy)) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       const float al0 = mn0 == -INFINITY ? 1.f : fast_exp2(m0 - mn0);
       const float al1 = mn1 == -INFINITY ? 1.f : fast_exp2(m1 - mn1);
@@ -340,10 +347,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
     float p[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      p[nt][0] = fast_exp2(sc[nt][0] - mu0);
-      p[nt][1] = fast_exp2(sc[nt][1] - mu0);
-      p[nt][2] = fast_exp2(sc[nt][2] - mu1);
-      p[nt][3] = fast_exp2(sc[nt][3] - mu1);
+      p[nt][0] = fast_exp2(fmaf(sc[nt][0], sl2, -mu0));
+      p[nt][1] = fast_exp2(fmaf(sc[nt][1], sl2, -mu0));
+      p[nt][2] = fast_exp2(fmaf(sc[nt][2], sl2, -mu1));
+      p[nt][3] = fast_exp2(fmaf(sc[nt][3], sl2, -mu1));
     }
     l0 += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
     l1 += (p[0][2] + p[0][3]) + (p[1][2] + p[1][3]);

@@ -112,48 +112,29 @@ int num_sms() {
   return n;
 }
 
-// ---- attention launch configuration (warps per CTA x stages per warp) ----
-struct K4Cfg {
-  int nw, ns;
-};
-K4Cfg k4_cfg() {
-  static K4Cfg c = [] {
-    K4Cfg d{8, 2};
-    if (const char* e = std::getenv("SGQA_K4_CFG")) {
-      int a = 0, b = 0;
-      if (std::sscanf(e, "%dx%d", &a, &b) == 2 && ((a == 8 && b == 2) || (a == 6 && b == 3) || (a == 4 && b == 4)))
-        d = K4Cfg{a, b};
-    }
-    return d;
-  }();
-  return c;
-}
+// ---- attention launch: 8 warps (units) per CTA, two stages each ----
+constexpr int kK4Warps = 8;
+size_t k4_smem(int nw) { return (size_t)nw * 2 * K4_STAGE + (size_t)nw * 2 * 8 + 1024; }
 
-size_t k4_smem(int nw, int ns) { return (size_t)nw * ns * K4_STAGE + (size_t)nw * ns * 8 + 1024; }
-
-template <int NW, int NS, bool TMA>
+template <bool TMA>
 cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
                         cudaStream_t st) {
-  const size_t smem = k4_smem(NW, NS);
+  const size_t smem = k4_smem(kK4Warps);
   static bool attr = false;
   if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k4_sparse_attn<NW, NS, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k4_sparse_attn<kK4Warps, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int64_t grid = cdiv(n_units, NW);
-  k4_sparse_attn<NW, NS, TMA><<<(unsigned)grid, NW * 32, smem, st>>>(a, tk, tv);
+  const int64_t grid = cdiv(n_units, kK4Warps);
+  k4_sparse_attn<kK4Warps, TMA><<<(unsigned)grid, kK4Warps * 32, smem, st>>>(a, tk, tv);
   return cudaGetLastError();
 }
 
 cudaError_t launch_k4(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units, bool tma,
                       cudaStream_t st) {
-  if (!tma) return launch_k4_t<8, 2, false>(a, tk, tv, n_units, st);
-  const K4Cfg c = k4_cfg();
-  if (c.nw == 6) return launch_k4_t<6, 3, true>(a, tk, tv, n_units, st);
-  if (c.nw == 4) return launch_k4_t<4, 4, true>(a, tk, tv, n_units, st);
-  return launch_k4_t<8, 2, true>(a, tk, tv, n_units, st);
+  return tma ? launch_k4_t<true>(a, tk, tv, n_units, st) : launch_k4_t<false>(a, tk, tv, n_units, st);
 }
 
 // K and V cache maps for the attention kernels: dims {64, tokens, 3 chunks} with strides
