@@ -37,6 +37,7 @@ constexpr int K4_D = 192;
 constexpr int K4_UNITS = K4_D / 8;            // 16-byte units per row: 24
 constexpr uint32_t K4_TILE = 16 * K4_D * 2;   // 16 keys x 192 bf16 = 6144 B
 constexpr uint32_t K4_STAGE = 2 * K4_TILE;    // K + V
+constexpr int K4_SEL_CACHE = 512;             // selection entries a warp keeps in shared memory
 
 struct K4Args {
   const __nv_bfloat16* q;       // [rows, H, D]
@@ -115,19 +116,28 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const int32_t s_end = s_begin + per_split < n_st ? s_begin + per_split : n_st;
   const int64_t row_base = (int64_t)g * a.ctx_cap + kvo;  // cache row of token 0 of this unit
 
-  // Block j of the selection: -1 past the count, -2 for an index outside 0..bt.  The
-  // selection is read 32 entries at a time into a register (`cur` for chunk ccur, `nxt`
-  // for the chunk after it, loaded a chunk ahead) and handed out by shuffles.
-  auto load_chunk = [&](int32_t c) -> int32_t {
-    const int32_t j = c * 32 + (int32_t)lane;
+  // Block j of the selection: -1 past the count, -2 for an index outside 0..bt.  Rows of
+  // up to K4_SEL_CACHE entries are copied once into this warp's shared-memory table, so a
+  // lookup is one broadcast shared load; longer rows read the global array.
+  int32_t* selc = reinterpret_cast<int32_t*>(smem + NW * NSTAGE * K4_STAGE + NW * NSTAGE * 8) + warp * K4_SEL_CACHE;
+  const uint32_t selc_s = smem_u32(selc);
+  const bool cached = !a.dense && cnt <= K4_SEL_CACHE;
+  if (cached) {
+#pragma unroll
+    for (int m = 0; m < K4_SEL_CACHE / 32; ++m) {
+      const int32_t j = m * 32 + (int32_t)lane;
+      const int32_t v = j < cnt ? __ldg(sel + j) : -1;
+      asm volatile("st.shared.b32 [%0], %1;" ::"r"(selc_s + 4u * j), "r"(v) : "memory");
+    }
+  }
+  __syncwarp();
+  auto lookup = [&](int32_t j) -> int32_t {  // every lane calls it with the same j
     if (j >= cnt) return -1;
-    return a.dense ? j : __ldg(sel + j);
-  };
-  int32_t ccur = (s_begin * bps) >> 5;
-  int32_t cur = load_chunk(ccur), nxt = load_chunk(ccur + 1);
-  auto blk = [&](int32_t j) -> int32_t {  // every lane calls it with the same j
-    const int32_t v = __shfl_sync(0xffffffffu, (j >> 5) == ccur ? cur : nxt, j & 31);
-    if (j >= cnt) return -1;
+    int32_t v;
+    if (cached)
+      asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(selc_s + 4u * j) : "memory");
+    else
+      v = a.dense ? j : __ldg(sel + j);
     return (v >= 0 && v <= bt) ? v : -2;
   };
 
@@ -174,18 +184,14 @@ __global__ void __launch_bounds__(NW * 32, 1)
   for (int jx = 0; jx < 4; ++jx)
     v_off[jx] = ((lane >> 3) & 1) * 3072 + kr * 128 + (((((lane >> 4) ^ kr)) ^ (2u * jx)) << 4);
 
-  // ---- stage loader (every lane calls it); nb0/nb1 keep the blocks of the stage issued
-  // last, which the next iteration masks with ----
-  int32_t nb0 = 0, nb1 = 0;
-  auto issue = [&](int32_t s) {
+  // ---- stage loader.  TMA: lane 0 fetches stage s from blocks (b0, b1) looked up one
+  // iteration earlier, so no shuffle latency sits in front of the copies. ----
+  auto issue = [&](int32_t s, int32_t b0, int32_t b1) {
     const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
     const uint32_t ks_addr = wbase + slot * K4_STAGE;
     const uint32_t vs_addr = ks_addr + K4_TILE;
     if (TMA) {
       // B = 8: two blocks of 8 keys; B = 16: the two halves of one block
-      int32_t b0 = blk(s * bps), b1 = bps == 2 ? blk(s * bps + 1) : b0;
-      nb0 = b0;
-      nb1 = b1;
       if (b0 < 0) b0 = bt;  // unused / invalid slot: fetch the own block, masked below
       if (b1 < 0) b1 = bt;
       if (lane == 0) {
@@ -236,23 +242,39 @@ __global__ void __launch_bounds__(NW * 32, 1)
     return true;
   };
 
-  for (int s = 0; s < NSTAGE - 1; ++s)
-    if (s_begin + s < s_end) { issue(s_begin + s); issued = s_begin + s + 1; }
-    else if (!TMA) cp_async_commit();
+  // nb0/nb1: blocks of the stage issued last (masked by the next iteration); pb0/pb1:
+  // blocks of the stage to issue next
+  int32_t nb0 = 0, nb1 = 0, pb0 = 0, pb1 = 0;
+  auto look_stage = [&](int32_t s) {
+    if (TMA && s < s_end) {
+      pb0 = lookup(s * bps);
+      pb1 = bps == 2 ? lookup(s * bps + 1) : pb0;
+    }
+  };
+  look_stage(s_begin);
+  if (s_begin < s_end) {
+    issue(s_begin, pb0, pb1);
+    nb0 = pb0;
+    nb1 = pb1;
+    issued = s_begin + 1;
+  } else if (!TMA) {
+    cp_async_commit();
+  }
+  look_stage(s_begin + 1);
 
   for (int32_t s = s_begin; s < s_end; ++s) {
-    // move the selection registers along once this stage's blocks leave chunk ccur
-    if (((s * bps) >> 5) != ccur) {
-      ++ccur;
-      cur = nxt;
-      nxt = load_chunk(ccur + 1);
-    }
-    // blocks of this stage (fetched by the previous issue) and whether all are valid and
-    // strictly before the own block
+    // blocks of this stage and whether all are valid and strictly before the own block
     const int32_t cb0 = nb0, cb1 = nb1;
-    // prefetch into the slot stage s-1 has released
-    if (s + NSTAGE - 1 < s_end) { issue(s + NSTAGE - 1); issued = s + NSTAGE; }
-    else if (!TMA) cp_async_commit();
+    // prefetch into the slot stage s-1 has released, then look up the stage after it
+    if (s + 1 < s_end) {
+      issue(s + 1, pb0, pb1);
+      nb0 = pb0;
+      nb1 = pb1;
+      issued = s + 2;
+      look_stage(s + 2);
+    } else if (!TMA) {
+      cp_async_commit();
+    }
     bool fast = true;
     if (TMA) {
       fast = cb0 >= 0 && cb0 < bt && cb1 >= 0 && cb1 < bt;

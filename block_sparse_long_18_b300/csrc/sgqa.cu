@@ -114,7 +114,7 @@ int num_sms() {
 
 // ---- attention launch: 8 warps (units) per CTA, two stages each ----
 constexpr int kK4Warps = 8;
-size_t k4_smem(int nw) { return (size_t)nw * 2 * K4_STAGE + (size_t)nw * 2 * 8 + 1024; }
+size_t k4_smem(int nw) { return (size_t)nw * 2 * K4_STAGE + (size_t)nw * 2 * 8 + (size_t)nw * K4_SEL_CACHE * 4 + 1024; }
 
 template <bool TMA>
 cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
