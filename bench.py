@@ -38,9 +38,9 @@ METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline p
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
 # DRAM bytes (read + write) per K4 launch from an ncu capture of the current kernel
-# (profiles/k4_sparse_attn_l128k_tail.md): 7.52 GB for the 65,536 (row, group) units of
-# the l128k_tail workload, scaled to the full 128K launch by kept blocks (x7.88).
-K4_TRAFFIC = {"l128k_tail": 7.517e9, "l128k": 59.2e9}
+# (profiles/k4_sparse_attn_l128k_tail.md): 6.83 GB for the 65,536 (row, group) units of
+# the l128k_tail workload, scaled to the full 128K launch by kept blocks (x7.875).
+K4_TRAFFIC = {"l128k_tail": 6.833e9, "l128k": 53.8e9}
 K4_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, l128k_tail capture (scaled for l128k)"
 
 
