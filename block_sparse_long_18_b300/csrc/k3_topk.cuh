@@ -25,6 +25,8 @@
 // so the tie rule carries over.  A STREAM instance (tiles of NT*PER re-read for every pass)
 // serves rows whose merge lists would not fit in registers either.
 #pragma once
+#include <type_traits>
+
 #include "ptx.cuh"
 
 namespace sgqa {
@@ -55,10 +57,12 @@ enum K3Mode : int {
   K3_MERGE = 2    // candidates = the row's segment pairs; writes the final selection
 };
 
+// Order-preserving unsigned key of a score.  Adding +0 turns -0 into +0 (round to
+// nearest; denormals are kept, the library is built without flush-to-zero), then negative
+// values have all bits flipped and non-negative ones the sign bit set.
 __device__ __forceinline__ uint32_t score_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u << 1) == 0) u = 0;  // -0 -> +0
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
 }
 
 // Inclusive warp scan.
@@ -267,82 +271,109 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
 
   // ---- compaction in ascending index order ----
   // A key is kept if its masked value exceeds the prefix, or equals it and its rank among
-  // the equal keys (in index order) is at least `skip`.
+  // the equal keys (in index order) is at least `skip`.  Without ties to break (skip = 0,
+  // the usual case) a key is kept iff its masked value is at least the prefix.
   const uint32_t skip = eq_count - need_rem;
-  uint32_t out_base = 0, tie_base = 0;
-  for (int tile = 0; tile < n_tiles; ++tile) {
-    if (STREAM) load_tile(tile);
-    // per (j, lane): packed counts (greater << 16 | equal) of its 4 keys, scanned per warp
-    uint32_t wex[NJ];
+  auto compact = [&](auto ties_tag) {
+    constexpr bool TIES = decltype(ties_tag)::value;
+    uint32_t out_base = 0, tie_base = 0;
+    for (int tile = 0; tile < n_tiles; ++tile) {
+      if (STREAM) load_tile(tile);
+      // per (j, lane): counts of its 4 keys (TIES: packed greater << 16 | equal), scanned
+      // per warp
+      uint32_t wex[NJ];
 #pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      uint32_t c = 0;
+      for (int j = 0; j < NJ; ++j) {
+        uint32_t c = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t kh = key[4 * j + e] & pmask;
-        c += kh > prefix ? (1u << 16) : (kh == prefix ? 1u : 0u);
-      }
-      const uint32_t inc = warp_incl_scan(c);
-      wex[j] = inc - c;
-      if (lane == 31) jw_cnt[j * NW + warp] = inc;
-    }
-    __syncthreads();
-    // exclusive scan over the NJ*NW (group, warp) totals in index order (j major)
-    if (warp == 0) {
-      constexpr int PERL = (NJ * NW + 31) / 32;
-      uint32_t v[PERL];
-      uint32_t s = 0;
-#pragma unroll
-      for (int q = 0; q < PERL; ++q) {
-        const int idx = lane * PERL + q;
-        v[q] = idx < NJ * NW ? jw_cnt[idx] : 0u;
-        s += v[q];
-      }
-      const uint32_t inc = warp_incl_scan(s);
-      uint32_t run = inc - s;
-#pragma unroll
-      for (int q = 0; q < PERL; ++q) {
-        const int idx = lane * PERL + q;
-        if (idx < NJ * NW) jw_cnt[idx] = run;
-        run += v[q];
-      }
-      if (lane == 31) warp_tot[0] = inc;  // tile total
-    }
-    __syncthreads();
-    const uint32_t tile_tot = warp_tot[0];
-    const uint32_t kept_prev = tie_base > skip ? tie_base - skip : 0u;  // ties kept by earlier tiles
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-      const uint32_t ex = jw_cnt[j * NW + warp] + wex[j];  // packed counts before this lane's group j
-      uint32_t ties_before = tie_base + (ex & 0xFFFFu);
-      uint32_t o = out_base + (ex >> 16) + (ties_before > skip ? ties_before - skip : 0u) - kept_prev;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int32_t slot = (int32_t)kidx(tile, j, e);
-        const uint32_t kh = key[4 * j + e] & pmask;
-        bool keep = kh > prefix;
-        if (kh == prefix) {
-          keep = ties_before >= skip;
-          ++ties_before;
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t kh = key[4 * j + e] & pmask;
+          if (TIES)
+            c += kh > prefix ? (1u << 16) : (kh == prefix ? 1u : 0u);
+          else
+            c += kh >= prefix ? 1u : 0u;
         }
-        if (keep) {
-          if (MODE == K3_SEGMENT) {
-            a.pair_key[r * pstride + (int64_t)seg * need + o] = key[4 * j + e];
-            a.pair_idx[r * pstride + (int64_t)seg * need + o] = (int32_t)(base + slot);
-          } else if (MODE == K3_MERGE) {
-            out[o] = __ldg(a.pair_idx + r * pstride + slot);
+        const uint32_t inc = warp_incl_scan(c);
+        wex[j] = inc - c;
+        if (lane == 31) jw_cnt[j * NW + warp] = inc;
+      }
+      __syncthreads();
+      // exclusive scan over the NJ*NW (group, warp) totals in index order (j major)
+      if (warp == 0) {
+        constexpr int PERL = (NJ * NW + 31) / 32;
+        uint32_t v[PERL];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int q = 0; q < PERL; ++q) {
+          const int idx = lane * PERL + q;
+          v[q] = idx < NJ * NW ? jw_cnt[idx] : 0u;
+          sum += v[q];
+        }
+        const uint32_t inc = warp_incl_scan(sum);
+        uint32_t run = inc - sum;
+#pragma unroll
+        for (int q = 0; q < PERL; ++q) {
+          const int idx = lane * PERL + q;
+          if (idx < NJ * NW) jw_cnt[idx] = run;
+          run += v[q];
+        }
+        if (lane == 31) warp_tot[0] = inc;  // tile total
+      }
+      __syncthreads();
+      const uint32_t tile_tot = warp_tot[0];
+      const uint32_t kept_prev = tie_base > skip ? tie_base - skip : 0u;  // ties kept by earlier tiles
+#pragma unroll
+      for (int j = 0; j < NJ; ++j) {
+        const uint32_t ex = jw_cnt[j * NW + warp] + wex[j];  // counts before this lane's group j
+        uint32_t ties_before = 0, o;
+        if (TIES) {
+          ties_before = tie_base + (ex & 0xFFFFu);
+          o = out_base + (ex >> 16) + (ties_before > skip ? ties_before - skip : 0u) - kept_prev;
+        } else {
+          o = out_base + ex;
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int32_t slot = (int32_t)kidx(tile, j, e);
+          const uint32_t kh = key[4 * j + e] & pmask;
+          bool keep;
+          if (TIES) {
+            keep = kh > prefix;
+            if (kh == prefix) {
+              keep = ties_before >= skip;
+              ++ties_before;
+            }
           } else {
-            out[o] = slot;
+            keep = kh >= prefix;
           }
-          ++o;
+          if (keep) {
+            if (MODE == K3_SEGMENT) {
+              a.pair_key[r * pstride + (int64_t)seg * need + o] = key[4 * j + e];
+              a.pair_idx[r * pstride + (int64_t)seg * need + o] = (int32_t)(base + slot);
+            } else if (MODE == K3_MERGE) {
+              out[o] = __ldg(a.pair_idx + r * pstride + slot);
+            } else {
+              out[o] = slot;
+            }
+            ++o;
+          }
         }
       }
+      if (TIES) {
+        const uint32_t t_gt = tile_tot >> 16, t_eq = tile_tot & 0xFFFFu;
+        out_base += t_gt + ((tie_base + t_eq > skip) ? (tie_base + t_eq - (tie_base > skip ? tie_base : skip)) : 0u);
+        tie_base += t_eq;
+      } else {
+        out_base += tile_tot;
+      }
+      __syncthreads();  // jw_cnt / warp_tot are rewritten by the next tile
     }
-    const uint32_t t_gt = tile_tot >> 16, t_eq = tile_tot & 0xFFFFu;
-    out_base += t_gt + ((tie_base + t_eq > skip) ? (tie_base + t_eq - (tie_base > skip ? tie_base : skip)) : 0u);
-    tie_base += t_eq;
-    __syncthreads();  // jw_cnt / warp_tot are rewritten by the next tile
-  }
+  };
+  // (the per-slice pass of the two-level top-k keeps one general path: registers are tight)
+  if (skip == 0 && MODE != K3_SEGMENT)
+    compact(std::integral_constant<bool, false>{});
+  else
+    compact(std::integral_constant<bool, true>{});
   if (tid == 0) {
     if (MODE == K3_SEGMENT) {
       a.pair_cnt[r * a.nseg + seg] = need;
