@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   __shared__ uint32_t wsum[2][NW];
   __shared__ uint32_t jw_cnt[NJ * NW];  // counts per (group j, warp), then their exclusive scan
   __shared__ uint32_t sh_digit, sh_above, sh_eq;
+  __shared__ uint32_t bitmap[STREAM ? 1 : NT * PER / 32];  // kept slots (no-tie compaction)
 
   constexpr int SEGLEN = NT * PER;  // candidates per segment (K3_SEGMENT)
   const int64_t r = MODE == K3_SEGMENT ? blockIdx.x / a.nseg : blockIdx.x;  // (group, row) of the launch
@@ -210,6 +211,9 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     hist2[0][b] = 0;
     hist2[1][b] = 0;
   }
+  if (!STREAM) {
+    for (int w = tid; w < NT * PER / 32; w += NT) bitmap[w] = 0;
+  }
   __syncthreads();
   uint32_t prefix = 0, pmask = 0;
   uint32_t need_rem = (uint32_t)need, eq_count = 0;
@@ -274,6 +278,36 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   // the equal keys (in index order) is at least `skip`.  Without ties to break (skip = 0,
   // the usual case) a key is kept iff its masked value is at least the prefix.
   const uint32_t skip = eq_count - need_rem;
+  // Register-resident rows without ties to break: the kept slots are marked in a bitmap
+  // and read out in ascending order (one word per thread, one block scan of the counts).
+  auto compact_bitmap = [&]() {
+#pragma unroll
+    for (int q = 0; q < PER; ++q) {
+      if ((key[q] & pmask) >= prefix) {
+        const uint32_t slot = (uint32_t)kidx(0, q >> 2, q & 3);
+        atomicOr(&bitmap[slot >> 5], 1u << (slot & 31));
+      }
+    }
+    __syncthreads();
+    uint32_t w = bitmap[tid];
+    uint32_t total;
+    uint32_t o = k3_block_excl_scan<NT>((uint32_t)__popc(w), warp_tot, total);
+    while (w != 0u) {
+      const int32_t slot = (int32_t)(tid * 32 + (uint32_t)__ffs(w) - 1u);
+      w &= w - 1u;
+      if (o < (uint32_t)need) {  // exactly need bits are set
+        if (MODE == K3_SEGMENT) {
+          a.pair_key[r * pstride + (int64_t)seg * need + o] = score_key(__ldg(row + base + slot));
+          a.pair_idx[r * pstride + (int64_t)seg * need + o] = (int32_t)(base + slot);
+        } else if (MODE == K3_MERGE) {
+          out[o] = __ldg(a.pair_idx + r * pstride + slot);
+        } else {
+          out[o] = slot;
+        }
+      }
+      ++o;
+    }
+  };
   auto compact = [&](auto ties_tag) {
     constexpr bool TIES = decltype(ties_tag)::value;
     uint32_t out_base = 0, tie_base = 0;
@@ -370,7 +404,9 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     }
   };
   // (the per-slice pass of the two-level top-k keeps one general path: registers are tight)
-  if (skip == 0 && MODE != K3_SEGMENT)
+  if (!STREAM && skip == 0)
+    compact_bitmap();
+  else if (skip == 0 && MODE != K3_SEGMENT)
     compact(std::integral_constant<bool, false>{});
   else
     compact(std::integral_constant<bool, true>{});
