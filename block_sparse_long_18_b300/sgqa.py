@@ -255,29 +255,86 @@ def prefill(prm: Params, q, k, v, gate, q_proxy, k_proxy, q_start: int = 0, k_bl
 
 
 class HostPrefill:
-    """End-to-end prefill from HOST (pinned) tensors: copies the inputs to the device on
-    one stream, runs the layer, and copies the output back.  Device buffers are kept
-    between calls."""
+    """End-to-end prefill from HOST (pinned) tensors, pipelined over chunks of query rows.
 
-    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda"):
-        self.prm = prm
-        self.plan = PrefillPlan(prm, T, ctx_cap, q_start, device)
+    Chunk j (rows [a, b)) needs the K/V/proxy cache up to position q_start + b only
+    (causality), so its copies in, its layer call (a chunked prefill at q_start + a) and
+    its output copy back run on three streams and overlap with the neighbouring chunks:
+    copy-in of chunk j+1 and copy-out of chunk j-1 proceed while chunk j is computed.
+    Device buffers are kept between calls.  The calling stream (or the current one) waits
+    for the last copy back, so events recorded on it around `run` time the whole job."""
+
+    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda", chunk_rows: int = 8192):
+        self.prm, self.T, self.ctx_cap, self.q_start = prm, T, ctx_cap, q_start
         G, H, D, P = prm.num_kv_groups, prm.num_kv_groups * prm.heads_per_group, prm.head_dim, prm.proxy_dim
+        B, k = prm.block_size, prm.top_k_blocks
+        self.R = max(B, min(T, chunk_rows) // B * B)  # rows per chunk, a multiple of B
         mk = lambda *s: torch.empty(s, dtype=BF16, device=device)
-        self.d = dict(q=mk(T, H, D), k=mk(G, ctx_cap, D), v=mk(G, ctx_cap, D), gate=mk(T, H, D), q_proxy=mk(G, T, P),
+        self.d = dict(q=mk(T, H, D), k=mk(G, ctx_cap, D), v=mk(G, ctx_cap, D), gate=mk(T, H, D),
                       k_proxy=mk(G, ctx_cap, P))
+        # q_proxy per chunk, contiguous [G, rows, P]; two buffers so that chunk j+1's copy
+        # overlaps chunk j's call
+        self.qp = [torch.empty(G * self.R * P, dtype=BF16, device=device) for _ in range(2)]
+        self.k_blk = torch.zeros((G, (ctx_cap + B - 1) // B, P), dtype=BF16, device=device)
+        self.sel = torch.empty(G * self.R * k, dtype=I32, device=device)
+        self.cnt = torch.empty(G * self.R, dtype=I32, device=device)
+        self.out = mk(T, H, D)
+        self.lse = torch.empty((T, H), dtype=F32, device=device)
+        self.ws = torch.empty(sgqa_workspace_bytes(prm, SGQA_OP_PREFILL, self.R, q_start + T), dtype=torch.uint8,
+                              device=device)
         self.out_host = torch.empty((T, H, D), dtype=BF16, pin_memory=True)
+        self.s_in = torch.cuda.Stream(device)
+        self.s_out = torch.cuda.Stream(device)
 
     def h2d_bytes(self) -> int:
-        return sum(t.numel() * t.element_size() for t in self.d.values())
+        G, P = self.prm.num_kv_groups, self.prm.proxy_dim
+        return sum(t.numel() * t.element_size() for t in self.d.values()) + G * self.T * P * 2
 
     def d2h_bytes(self) -> int:
         return self.out_host.numel() * self.out_host.element_size()
 
     def run(self, host: dict, stream=None) -> torch.Tensor:
-        for name, t in self.d.items():
-            t.copy_(host[name], non_blocking=True)
-        d = self.d
-        self.plan.run(d["q"], d["k"], d["v"], d["gate"], d["q_proxy"], d["k_proxy"], stream)
-        self.out_host.copy_(self.plan.out, non_blocking=True)
+        prm, d, R, q0 = self.prm, self.d, self.R, self.q_start
+        G, P, k = prm.num_kv_groups, prm.proxy_dim, prm.top_k_blocks
+        comp = stream if stream is not None else torch.cuda.current_stream()
+        begin = torch.cuda.Event()
+        begin.record(comp)
+        self.s_in.wait_event(begin)
+        self.s_out.wait_event(begin)
+        released = []  # per chunk: its layer call has finished (its q_proxy buffer is free)
+        ctx_done = 0   # cache positions copied so far
+        for j, a in enumerate(range(0, self.T, R)):
+            b = min(self.T, a + R)
+            rows = b - a
+            qp = self.qp[j % 2][:G * rows * P].view(G, rows, P)
+            with torch.cuda.stream(self.s_in):
+                if j >= 2:
+                    self.s_in.wait_event(released[j - 2])
+                hi = q0 + b  # cache positions this chunk attends to
+                for name in ("k", "v", "k_proxy"):
+                    for g in range(G):
+                        d[name][g, ctx_done:hi].copy_(host[name][g, ctx_done:hi], non_blocking=True)
+                d["q"][a:b].copy_(host["q"][a:b], non_blocking=True)
+                d["gate"][a:b].copy_(host["gate"][a:b], non_blocking=True)
+                for g in range(G):
+                    qp[g].copy_(host["q_proxy"][g, a:b], non_blocking=True)
+                copied = torch.cuda.Event()
+                copied.record(self.s_in)
+            comp.wait_event(copied)
+            if j == 0 and q0 > 0:  # blocks of the cached prefix
+                sgqa_build_block_index(prm, d["k_proxy"], 0, q0, self.k_blk, comp)
+            sgqa_prefill(prm, d["q"][a:b], d["k"], d["v"], d["gate"][a:b], qp, d["k_proxy"], q0 + a, self.k_blk,
+                         self.sel[:G * rows * k].view(G, rows, k), self.cnt[:G * rows].view(G, rows), self.out[a:b],
+                         self.lse[a:b], self.ws, comp)
+            done = torch.cuda.Event()
+            done.record(comp)
+            released.append(done)
+            ctx_done = hi
+            self.s_out.wait_event(done)
+            with torch.cuda.stream(self.s_out):
+                self.out_host[a:b].copy_(self.out[a:b], non_blocking=True)
+        end = torch.cuda.Event()
+        end.record(self.s_out)
+        comp.wait_event(end)
         return self.out_host
+

@@ -222,6 +222,23 @@ def test_small_workspace_many_passes(sg):
     assert torch.equal(idx, res.sel_idx) and torch.equal(cnt, res.sel_cnt)
 
 
+@pytest.mark.parametrize("q_start", [0, 1000])
+def test_host_prefill_pipeline_equals_device_prefill(sg, q_start):
+    """The end-to-end API (pinned host tensors, chunks of rows pipelined over three
+    streams) gives bit-identical outputs to one prefill call on device tensors."""
+    wl = gen.small_workload(T=2600, G=2, Hg=16, B=8, k=24, planted=True, q_start=q_start)
+    inp = _to_cuda(gen.make_inputs(wl, seed=11))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    hp = sg.HostPrefill(prm, wl.T, wl.C, wl.q_start, chunk_rows=1024)  # three chunks
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "gate", "q_proxy", "k_proxy")}
+    for _ in range(2):  # a second run reuses every buffer
+        out = hp.run(host)
+        torch.cuda.synchronize()
+        assert sg.sgqa_get_device_error() == 0
+        assert torch.equal(out, res.out.cpu())
+
+
 # ---------------------------------------------------------------------------------------
 # error paths on the device (no fault: bounded waits and checked indices)
 # ---------------------------------------------------------------------------------------
