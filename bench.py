@@ -365,7 +365,7 @@ def run_sgqa(args, rank, world, local_rank):
         e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world, dev)
         e2e = {"value": job_value(wl.T, world, e_ms), "unit": "tokens/s", "ms_per_step": round(e_ms, 3),
                "h2d_bytes_per_step": hp.h2d_bytes(), "d2h_bytes_per_step": hp.d2h_bytes(),
-               "api": "HostPrefill.run -> sgqa_prefill per 8,192-row chunk, copies overlapped on two more streams"}
+               "api": "HostPrefill.run -> sgqa_prefill per 4,096-row chunk, copies overlapped on two more streams"}
         del hp, host
 
     # ---- CPU baseline (oracle), rank 0 only ----

@@ -264,7 +264,7 @@ class HostPrefill:
     Device buffers are kept between calls.  The calling stream (or the current one) waits
     for the last copy back, so events recorded on it around `run` time the whole job."""
 
-    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda", chunk_rows: int = 8192):
+    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda", chunk_rows: int = 4096):
         self.prm, self.T, self.ctx_cap, self.q_start = prm, T, ctx_cap, q_start
         G, H, D, P = prm.num_kv_groups, prm.num_kv_groups * prm.heads_per_group, prm.head_dim, prm.proxy_dim
         B, k = prm.block_size, prm.top_k_blocks
