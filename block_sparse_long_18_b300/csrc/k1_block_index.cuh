@@ -44,9 +44,14 @@ __global__ void __launch_bounds__(256) k1_block_index(K1Args a) {
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     const uint4* src = reinterpret_cast<const uint4*>(a.k_proxy + ((g * a.ctx_cap + first) * a.P)) + pv;
-    for (int64_t j = 0; j < n; ++j) {
-      uint4 w = __ldg(src + j * vec_per_row);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+    // all (at most 16) token loads are issued before the first add, then summed in order
+    uint4 wv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) wv[j] = j < n ? __ldg(src + j * vec_per_row) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j >= n) break;
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&wv[j]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float2 f = __bfloat1622float2(h[e]);
@@ -100,9 +105,14 @@ __global__ void __launch_bounds__(256) k1_block_index_seq(const __grid_constant_
     for (int e = 0; e < 8; ++e) acc[e] = 0.f;
     const uint4* src =
         reinterpret_cast<const uint4*>(a.k_proxy + (((int64_t)g * a.total + a.kv_off[s] + first) * a.P)) + pv;
-    for (int64_t j = 0; j < n; ++j) {
-      uint4 w = __ldg(src + j * vec_per_row);
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+    // all (at most 16) token loads are issued before the first add, then summed in order
+    uint4 wv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) wv[j] = j < n ? __ldg(src + j * vec_per_row) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j >= n) break;
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&wv[j]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         float2 f = __bfloat1622float2(h[e]);

@@ -2,7 +2,8 @@
 // against that sequence's earlier block proxies.  Same definition as the prefill indexer
 // (a plain dot product, fp32 accumulation; ai4snews item, Interpretation para 2), but with
 // a single query row it is a matrix-vector product that streams the block-proxy cache
-// from HBM: one warp reads one 512-byte block row per load (P = 256), four rows in flight.
+// from HBM: one warp reads one 512-byte block row per load (P = 256), eight rows per step
+// with the next step's eight already in flight.
 #pragma once
 #include "ptx.cuh"
 
@@ -43,17 +44,26 @@ __global__ void __launch_bounds__(256) k2d_decode_index(const __grid_constant__ 
   const int64_t b_lo = (int64_t)blockIdx.x * a.rows_per_cta;
   int64_t b_hi = b_lo + a.rows_per_cta;
   if (b_hi > n) b_hi = n;
-  for (int64_t b0 = b_lo + warp * 4; b0 < b_hi; b0 += 8 * 4) {
-    float acc[4];
-    uint4 w[4];
+  // each warp takes 8 consecutive rows per step; the next step's rows are loaded before
+  // this step's dot products are reduced, so 16 rows (8 KB) per warp are in flight
+  constexpr int RW = 8;
+  auto load = [&](int64_t b0, uint4 (&w)[RW]) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < RW; ++r) {
       w[r] = make_uint4(0, 0, 0, 0);
       if (active && b0 + r < b_hi) w[r] = __ldg(reinterpret_cast<const uint4*>(base + (b0 + r) * a.P) + lane);
     }
+  };
+  const int64_t step = 8 * RW;  // 8 warps
+  uint4 cur[RW], nxt[RW];
+  int64_t b0 = b_lo + warp * RW;
+  if (b0 < b_hi) load(b0, cur);
+  for (; b0 < b_hi; b0 += step) {
+    if (b0 + step < b_hi) load(b0 + step, nxt);
+    float acc[RW];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w[r]);
+    for (int r = 0; r < RW; ++r) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&cur[r]);
       float sum = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -66,13 +76,16 @@ __global__ void __launch_bounds__(256) k2d_decode_index(const __grid_constant__ 
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+      for (int r = 0; r < RW; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
     }
-    if (lane == 0) {
+    if (lane < RW && b0 + lane < b_hi) {
+      float v = acc[0];
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
-        if (b0 + r < b_hi) out[b0 + r] = acc[r];
+      for (int r = 1; r < RW; ++r) v = lane == r ? acc[r] : v;
+      out[b0 + lane] = v;
     }
+#pragma unroll
+    for (int r = 0; r < RW; ++r) cur[r] = nxt[r];
   }
 }
 

@@ -502,7 +502,7 @@ struct K4CombineArgs {
   __nv_bfloat16* out;
   float* lse;
   int64_t rows;
-  int32_t G, Hg, H, nsplit, gate_per_dim;
+  int32_t G, Hg, H, nsplit, gate_per_dim;  // nsplit <= 32 (one lane per split)
 };
 
 __global__ void __launch_bounds__(256) k4_combine(const K4CombineArgs a) {
@@ -514,22 +514,33 @@ __global__ void __launch_bounds__(256) k4_combine(const K4CombineArgs a) {
   const int64_t gr = wid / a.Hg;           // = g * rows + i
   const int g = (int)(gr / a.rows);
   const int64_t i = gr % a.rows;
-  float M = -INFINITY;
-  for (int s = 0; s < a.nsplit; ++s) {
-    const float* ml = a.part_ml + ((gr * a.nsplit + s) * 16 + h) * 2;
-    if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+  // lane s holds split s (nsplit <= 32): its (m, l), the maximum over splits with mass and
+  // its weight exp2(m_s - M)
+  float ms = -INFINITY, ls = 0.f;
+  if ((int)lane < a.nsplit) {
+    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + ((gr * a.nsplit + lane) * 16 + h) * 2);
+    if (ml.y > 0.f) {
+      ms = ml.x;
+      ls = ml.y;
+    }
   }
-  float L = 0.f;
-  float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int s = 0; s < a.nsplit; ++s) {
-    const int64_t u = gr * a.nsplit + s;
-    const float* ml = a.part_ml + (u * 16 + h) * 2;
-    if (!(ml[1] > 0.f)) continue;
-    const float w = fast_exp2(ml[0] - M);
-    L += w * ml[1];
-    const float* po = a.part_o + (u * 16 + h) * K4_D;
+  float M = ms;
 #pragma unroll
-    for (int e = 0; e < 6; ++e) acc[e] += w * po[lane + 32 * e];
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float ws = ls > 0.f ? fast_exp2(ms - M) : 0.f;
+  float L = ws * ls;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  // O: lane d-slice (d = lane + 32 e), summed over the splits with their weights
+  float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float* po = a.part_o + (gr * a.nsplit * 16 + h) * K4_D + lane;
+#pragma unroll 8
+  for (int s = 0; s < a.nsplit; ++s) {
+    const float w = __shfl_sync(0xffffffffu, ws, s);
+    if (w == 0.f) continue;  // warp-uniform
+    const float* ps = po + (int64_t)s * 16 * K4_D;
+#pragma unroll
+    for (int e = 0; e < 6; ++e) acc[e] = fmaf(w, __ldg(ps + 32 * e), acc[e]);
   }
   const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
   const int64_t head = i * a.H + (int64_t)g * a.Hg + h;
