@@ -539,7 +539,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["sgqa", "reference"], default="sgqa")
-    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "chunk1m", "l128k_tail", "decode"])
+    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "l128k_b1", "chunk1m", "l128k_tail", "decode"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-coverage", action="store_true")
