@@ -142,17 +142,22 @@ class ClockSampler:
 # CPU baseline: the oracle, as it stands, on a bounded sample of the workload
 # ---------------------------------------------------------------------------------------
 
-def cpu_oracle_rate(inp_host, wl, n_rows, seed=0):
+def cpu_oracle_rate(inp_host, wl, n_rows, seed=0, kb_t=None):
     """Oracle time for n_rows query tokens (all groups: indexer + top-k + attention), plus
-    its block-index pass prorated to those rows.  Returns (tokens/s, seconds, rows, cores)."""
+    its block-index pass prorated to those rows.  kb_t: a block index already built by the
+    oracle and the seconds it took (reused across samples).  Returns (tokens/s, seconds,
+    rows, cores)."""
     import oracle
 
     rng = np.random.default_rng(seed)
     rows = np.sort(rng.choice(wl.T, size=n_rows, replace=False)).astype(np.int64)
     d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k)
-    t0 = time.perf_counter()
-    kb = oracle.block_index(inp_host["k_proxy"], wl.B, 0, wl.C)
-    t_k1 = time.perf_counter() - t0
+    if kb_t is None:
+        t0 = time.perf_counter()
+        kb = oracle.block_index(inp_host["k_proxy"], wl.B, 0, wl.C)
+        t_k1 = time.perf_counter() - t0
+    else:
+        kb, t_k1 = kb_t
     t0 = time.perf_counter()
     for g in range(wl.G):
         pos = wl.q_start + rows
@@ -504,9 +509,14 @@ def run_reference(args, rank, world):
     inp = gen.make_inputs(wl, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
     hv = host_views(inp)
     del inp
-    rates, secs_all, n_rows = [], [], 8
+    # the block index is built once (its time is prorated into every sample); each step
+    # times the oracle on 64 query tokens drawn uniformly from the workload
+    t0 = time.perf_counter()
+    kb = oracle.block_index(hv["k_proxy"], wl.B, 0, wl.C)
+    kb_t = (kb, time.perf_counter() - t0)
+    rates, secs_all, n_rows = [], [], min(64, wl.T)
     for s in range(args.warmup + args.steps):
-        rate, secs, nrows, cores = cpu_oracle_rate(hv, wl, n_rows=n_rows, seed=100 + s)
+        rate, secs, nrows, cores = cpu_oracle_rate(hv, wl, n_rows=n_rows, seed=100 + s, kb_t=kb_t)
         if s >= args.warmup:
             rates.append(rate)
             secs_all.append(secs)
@@ -528,7 +538,8 @@ def run_reference(args, rank, world):
         "config": {"workload": f"{wl.name}: prefill T={wl.T}, context {wl.C}, G={wl.G} x Hg={wl.Hg}, D={wl.D}, "
                                f"P={wl.P}, block {wl.B}, top-k {wl.k}", "global_batch": 1, "seq_len": wl.T},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle", "cores": oracle.num_threads(),
-                         "sample": f"{n_rows} query tokens per step drawn from the workload, all groups, fp64"},
+                         "sample": f"{n_rows} query tokens per step drawn uniformly from the {wl.name} workload, all "
+                                   f"{wl.G} groups (indexer + top-k + attention, fp64), block-index pass prorated"},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
