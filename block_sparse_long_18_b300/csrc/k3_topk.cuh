@@ -107,7 +107,8 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   __shared__ uint32_t wsum[2][NW];
   __shared__ uint32_t jw_cnt[NJ * NW];  // counts per (group j, warp), then their exclusive scan
   __shared__ uint32_t sh_digit, sh_above, sh_eq;
-  __shared__ uint32_t bitmap[STREAM ? 1 : NT * PER / 32];  // kept slots (no-tie compaction)
+  __shared__ uint32_t bitmap[STREAM ? 1 : NT * PER / 32];  // kept slots
+  __shared__ uint32_t tiemap[STREAM ? 1 : NT * PER / 32];  // slots equal to the threshold key
 
   constexpr int SEGLEN = NT * PER;  // candidates per segment (K3_SEGMENT)
   const int64_t r = MODE == K3_SEGMENT ? blockIdx.x / a.nseg : blockIdx.x;  // (group, row) of the launch
@@ -212,7 +213,10 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     hist2[1][b] = 0;
   }
   if (!STREAM) {
-    for (int w = tid; w < NT * PER / 32; w += NT) bitmap[w] = 0;
+    for (int w = tid; w < NT * PER / 32; w += NT) {
+      bitmap[w] = 0;
+      tiemap[w] = 0;
+    }
   }
   __syncthreads();
   uint32_t prefix = 0, pmask = 0;
@@ -278,18 +282,31 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   // the equal keys (in index order) is at least `skip`.  Without ties to break (skip = 0,
   // the usual case) a key is kept iff its masked value is at least the prefix.
   const uint32_t skip = eq_count - need_rem;
-  // Register-resident rows without ties to break: the kept slots are marked in a bitmap
-  // and read out in ascending order (one word per thread, one block scan of the counts).
+  // Register-resident rows: the kept slots are marked in a bitmap and read out in
+  // ascending order (one word per thread, one block scan of the counts).  With ties to
+  // break, the keys equal to the threshold go to a second bitmap whose first `skip` set
+  // bits (the smallest indices) are dropped before the two are merged.
   auto compact_bitmap = [&]() {
 #pragma unroll
     for (int q = 0; q < PER; ++q) {
-      if ((key[q] & pmask) >= prefix) {
+      const uint32_t kh = key[q] & pmask;
+      if (kh >= prefix) {
         const uint32_t slot = (uint32_t)kidx(0, q >> 2, q & 3);
-        atomicOr(&bitmap[slot >> 5], 1u << (slot & 31));
+        atomicOr(skip != 0u && kh == prefix ? &tiemap[slot >> 5] : &bitmap[slot >> 5], 1u << (slot & 31));
       }
     }
     __syncthreads();
     uint32_t w = bitmap[tid];
+    if (skip != 0u) {  // block-uniform
+      uint32_t wt = tiemap[tid], ttot;
+      uint32_t rank = k3_block_excl_scan<NT>((uint32_t)__popc(wt), warp_tot, ttot);  // ties before this word
+      while (wt != 0u) {
+        const uint32_t bit = wt & (0u - wt);
+        wt ^= bit;
+        if (rank >= skip) w |= bit;
+        ++rank;
+      }
+    }
     uint32_t total;
     uint32_t o = k3_block_excl_scan<NT>((uint32_t)__popc(w), warp_tot, total);
     while (w != 0u) {
@@ -404,7 +421,7 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     }
   };
   // (the per-slice pass of the two-level top-k keeps one general path: registers are tight)
-  if (!STREAM && skip == 0)
+  if (!STREAM)
     compact_bitmap();
   else if (skip == 0 && MODE != K3_SEGMENT)
     compact(std::integral_constant<bool, false>{});
