@@ -44,9 +44,9 @@ def _run_decode(sg, inp, wl, prm):
     return k_blk, sel, cnt, out, lse
 
 
-def _check_sequences(inp, wl, res, seqs):
+def _check_sequences(inp, wl, res, seqs, gate_per_dim=1):
     k_blk, sel, cnt, out, lse = res
-    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k)
+    d = oracle.dims(wl.G, wl.Hg, wl.D, wl.P, wl.B, wl.k, gate_per_dim=gate_per_dim)
     for s in seqs:
         L, off = inp.ctx_len[s], inp.kv_off[s]
         nb = (L + wl.B - 1) // wl.B
@@ -74,6 +74,20 @@ def test_decode_ragged_small(sg):
     prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k)
     res = _run_decode(sg, inp, wl, prm)
     _check_sequences(inp, wl, res, range(wl.batch))
+
+
+@pytest.mark.parametrize("B,k,gate_per_dim", [(16, 8, 1), (4, 12, 1), (8, 10, 0)],
+                         ids=["B16", "B4_cp_async", "per_head_gate"])
+def test_decode_ragged_block_sizes_and_gates(sg, B, k, gate_per_dim):
+    """Ragged contexts with blocks of 16 (one block per stage), blocks of 4 (the cp.async
+    loader with split-K), and a per-head gate."""
+    wl = gen.Workload(f"dec_B{B}", T=1, C=0, G=2, Hg=16, B=B, k=k, batch=4, ctx_lo=1, ctx_hi=2500)
+    inp = gen.make_decode_inputs(wl, seed=6, device="cuda")
+    if not gate_per_dim:
+        inp.gate = inp.gate[:, :, 0].contiguous()  # [batch, H]
+    prm = sg.params(G=wl.G, Hg=wl.Hg, B=B, k=wl.k, gate_per_dim=gate_per_dim)
+    res = _run_decode(sg, inp, wl, prm)
+    _check_sequences(inp, wl, res, range(wl.batch), gate_per_dim=gate_per_dim)
 
 
 def test_decode_matches_prefill_last_row(sg):

@@ -96,6 +96,7 @@ SMALL = [
     dict(T=520, G=1, Hg=2, B=1, k=64),                    # token-level (B = 1) reference form
     dict(T=300, G=1, Hg=16, B=16, k=6),                   # B = 16
     dict(T=200, G=1, Hg=8, B=4, k=9),                     # B = 4 (cp.async loader)
+    dict(T=150, G=1, Hg=4, B=2, k=20),                    # B = 2
     dict(T=260, G=1, Hg=1, B=8, k=7, P=64),               # P = 64, single head
     dict(T=333, G=2, Hg=16, B=8, k=40, P=128, planted=True),
 ]
