@@ -1,0 +1,637 @@
+// k4u_attention.cuh -- gated sparse attention for 8 query rows at a time over the union of
+// their selected blocks, on the 5th-generation tensor cores (tcgen05, tensor memory).
+//
+// Same operation as k4_attention.cuh (ai.info article "StepFun Details Step 5 Preview's
+// 92-Block Agent Design", "Why StepFun chose 92 transformer blocks": Gated GQA; ai4snews
+// item "Step 5 Preview bets on depth over width", Interpretation para 2: sparse flash
+// attention over the selected blocks; phantomic12 entry: 4 KV groups x 16 heads, D = 192):
+//   for row i (position t), group g, head h of g:  J = { j in the row's selected blocks : j <= t }
+//   o = softmax_j(scale * q_h . k_j) . v_j ;  out = o * sigmoid(gate) ;  lse = log sum exp
+//
+// Unit = (KV group g, 8 consecutive query rows).  Its 8 rows x 16 heads = 128 (row, head)
+// pairs are the M of the MMA, one pair per tensor-memory lane.  The keys are the union U of
+// the 8 rows' selections in ascending block order: every union block is gathered once per
+// unit and serves every row that selected it; a row's scores outside its own selection
+// (and past its position inside its own block) are masked in the softmax.
+//   S [128 pairs x 128 keys]  = Q [128 x 192] (tensor memory) . K_chunk [128 keys x 192]^T
+//   O [128 pairs x 192]      += P [128 x 128] (tensor memory, bf16) . V_chunk [128 keys x 192]
+// Both products read A from tensor memory and B from shared memory, where each union block
+// lands by one TMA copy (box {64, 8, 3}) as three 1 KB swizzle atoms [D chunk][key][64]:
+// K-major for K (atoms 3 KB apart), MN-major for V.  The softmax is per thread: a (row,
+// head) pair owns its TMEM lane, so maxima, sums and the rare O rescale need no exchange.
+//
+// Tensor memory (512 columns): Q 0..95 (bf16 pairs), O 96..287, S 288..415, P 416..479.
+// Roles (one persistent CTA per SM, 12 warps, units dealt round-robin, group-major):
+//   warp 0     K producer: 16 copies per 128-key chunk into a 2-slot ring
+//   warp 3     V producer: the same for V
+//   warp 1     allocates tensor memory; one thread issues S(c), then O(c-1)
+//   warp 2     builds the next unit's union tables (double-buffered)
+//   warps 4-11 softmax + epilogue: thread = (row, head) = its TMEM lane, two warps per lane
+//              quarter (one per half of the keys); they also write the next unit's Q into
+//              tensor memory, so its first S overlaps this epilogue
+// Every wait is bounded; on expiry the CTA raises an abort flag, drains and returns.
+#pragma once
+#include "ptx.cuh"
+
+namespace sgqa {
+
+constexpr int K4U_D = 192;                          // head dimension
+constexpr int K4U_CB = 16;                          // union blocks per chunk (128 keys)
+constexpr uint32_t K4U_SLOT = K4U_CB * 3072;        // one chunk of K (or V): 48 KB
+constexpr int K4U_MAXU = 4096;                      // union capacity: 8 rows x 512 blocks
+constexpr int K4U_WIN = 16384;                      // blocks covered by one builder bitmap
+constexpr int K4U_MAX_BLOCKS = 65536;               // union entries are 16-bit block indices
+// one table buffer: union blocks (u16), per-row membership bits over union positions, meta
+constexpr uint32_t K4U_TB_UBLK = 0;
+constexpr uint32_t K4U_TB_RBITS = 2 * K4U_MAXU;              // uint32 [8][K4U_MAXU / 32]
+constexpr uint32_t K4U_TB_META = K4U_TB_RBITS + 8 * (K4U_MAXU / 8);  // int32: nU, own position [8]
+constexpr uint32_t K4U_TB = K4U_TB_META + 128;
+constexpr uint32_t K4U_K_OFF = 0;
+constexpr uint32_t K4U_V_OFF = 2 * K4U_SLOT;
+constexpr uint32_t K4U_T_OFF = 4 * K4U_SLOT;
+constexpr uint32_t K4U_BM_OFF = K4U_T_OFF + 2 * K4U_TB;      // uint32 [K4U_WIN / 32] window bitmap
+constexpr uint32_t K4U_PRE_OFF = K4U_BM_OFF + K4U_WIN / 8;   // uint32 [K4U_WIN / 32] prefix counts
+constexpr uint32_t K4U_X_OFF = K4U_PRE_OFF + K4U_WIN / 8;    // float [3][256]: chunk maxima (2 parities), row sums
+constexpr uint32_t K4U_BAR_OFF = K4U_X_OFF + 3 * 256 * 4;
+constexpr uint32_t K4U_SMEM = K4U_BAR_OFF + 512 + 1024;     // + barriers, flags, alignment
+constexpr int K4U_THREADS = 384;
+constexpr uint32_t K4U_COL_Q = 0, K4U_COL_O = 96, K4U_COL_S = 288, K4U_COL_P = 416;
+static_assert(K4U_SMEM <= 232448, "k4u shared memory");
+
+struct K4UArgs {
+  const __nv_bfloat16* q;     // [rows, H, D]
+  const __nv_bfloat16* gate;  // [rows, H, D] or [rows, H]
+  __nv_bfloat16* out;         // [rows, H, D]
+  float* lse;                 // [rows, H] or null
+  const int32_t* sel_idx;     // [G, rows, kcap], ascending, -1 padded
+  const int32_t* sel_cnt;     // [G, rows]
+  int64_t rows, pos0, ctx_cap;
+  int32_t G, H, kcap;         // 16 heads per group, blocks of 8, D = 192
+  float scale_log2;
+  int32_t gate_per_dim;
+  uint64_t wait_ns;
+};
+
+__global__ void __launch_bounds__(K4U_THREADS, 1)
+    k4u_sparse_attn(const __grid_constant__ K4UArgs a, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t k4u_smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(k4u_smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb0 = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K4U_BAR_OFF);
+  auto bar = [&](int idx) { return smem_u32(&bars[idx]); };
+  enum { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kTblFull = 8, kTblEmpty = 10, kSFull = 12, kSFree = 13,
+         kPFull = 14, kPvDone = 15, kQFull = 16, kQEmpty = 17, kOEmpty = 18, kFinal = 19 };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K4U_BAR_OFF + 256);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K4U_BAR_OFF + 260);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = lane_id();
+  const int64_t ntiles = (a.rows + 7) / 8;
+  const int64_t n_units = (int64_t)a.G * ntiles;
+  auto tbl = [&](uint32_t buf) { return smem + K4U_T_OFF + buf * K4U_TB; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kKFull + s), 1);
+      mbar_init(bar(kKEmpty + s), 1);
+      mbar_init(bar(kVFull + s), 1);
+      mbar_init(bar(kVEmpty + s), 1);
+      mbar_init(bar(kTblFull + s), 1);
+      mbar_init(bar(kTblEmpty + s), 11);  // K and V producers, MMA thread, 8 softmax warps
+    }
+    mbar_init(bar(kSFull), 1);
+    mbar_init(bar(kSFree), 8);
+    mbar_init(bar(kPFull), 8);
+    mbar_init(bar(kPvDone), 1);
+    mbar_init(bar(kQFull), 8);
+    mbar_init(bar(kQEmpty), 1);
+    mbar_init(bar(kOEmpty), 8);
+    mbar_init(bar(kFinal), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // lane 0 waits, the warp agrees on the outcome
+  auto warp_wait = [&](int b, uint32_t parity) -> bool {
+    bool r = true;
+    if (lane == 0) r = mbar_wait(bar(b), parity, a.wait_ns, abort_flag);
+    return __shfl_sync(0xffffffffu, r, 0) != 0;
+  };
+
+  if (warp == 2) {
+    // ------------------------------- union builder -------------------------------
+    // Per window of K4U_WIN blocks: mark every selected block in a bitmap, turn the bitmap
+    // into ascending union positions (prefix popcounts), then mark each row's entries in
+    // its membership bits.  The rows' own blocks are noted for the causal mask.
+    uint32_t* bm = reinterpret_cast<uint32_t*>(smem + K4U_BM_OFF);
+    uint32_t* pre = reinterpret_cast<uint32_t*>(smem + K4U_PRE_OFF);
+    uint32_t uc = 0;
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+      const uint32_t buf = uc & 1;
+      if (uc >= 2 && !warp_wait(kTblEmpty + buf, ((uc >> 1) - 1) & 1)) break;
+      const int32_t g = (int32_t)(u / ntiles);
+      const int64_t i0 = (u % ntiles) * 8;
+      uint8_t* T = tbl(buf);
+      uint16_t* ublk = reinterpret_cast<uint16_t*>(T + K4U_TB_UBLK);
+      uint32_t* rbits = reinterpret_cast<uint32_t*>(T + K4U_TB_RBITS);
+      int32_t* meta = reinterpret_cast<int32_t*>(T + K4U_TB_META);
+      int32_t cnt_l = 0, bt_l = -1;
+      if (lane < 8 && i0 + lane < a.rows) {
+        const int64_t i = i0 + lane;
+        bt_l = (int32_t)((a.pos0 + i) >> 3);
+        int32_t c = __ldg(a.sel_cnt + (int64_t)g * a.rows + i);
+        const int32_t cap = a.kcap < bt_l + 1 ? a.kcap : bt_l + 1;
+        if (c < 1 || c > cap) {
+          report_error(kErrBounds);
+          c = c < 1 ? 1 : cap;
+        }
+        cnt_l = c;
+      }
+      for (int w = lane; w < 8 * (K4U_MAXU / 32); w += 32) rbits[w] = 0u;
+      if (lane < 8) meta[1 + lane] = -1;
+      int32_t bmax = bt_l;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) bmax = max(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+      int32_t nU = 0;
+      for (int32_t wb = 0; wb <= bmax; wb += K4U_WIN) {
+        for (int w = lane; w < K4U_WIN / 32; w += 32) bm[w] = 0u;
+        __syncwarp();
+        for (int r0 = 0; r0 < 8; r0 += 2) {  // two rows' entries in flight at once
+          int32_t e[2][16];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r0 + rr);
+            const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i0 + r0 + rr) * a.kcap;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int32_t j = (int32_t)lane + 32 * k;
+              e[rr][k] = j < cnt ? __ldg(sel + j) : -1;
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r0 + rr);
+            const int32_t bt = __shfl_sync(0xffffffffu, bt_l, r0 + rr);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int32_t j = (int32_t)lane + 32 * k;
+              if (j >= cnt) continue;
+              const int32_t b = e[rr][k];
+              if (b < 0 || b > bt) {
+                if (wb == 0) report_error(kErrBounds);
+                continue;
+              }
+              const int32_t o = b - wb;
+              if (o >= 0 && o < K4U_WIN) atomicOr(&bm[o >> 5], 1u << (o & 31));
+            }
+          }
+        }
+        __syncwarp();
+        constexpr int WPL = K4U_WIN / 32 / 32;  // bitmap words per lane
+        uint32_t pc = 0;
+#pragma unroll
+        for (int k = 0; k < WPL; ++k) pc += __popc(bm[WPL * lane + k]);
+        uint32_t incl = pc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+          if ((int)lane >= o) incl += v;
+        }
+        uint32_t run = (uint32_t)nU + incl - pc;
+        for (int k = 0; k < WPL; ++k) {
+          const uint32_t wi = WPL * lane + k;
+          uint32_t bits = bm[wi];
+          pre[wi] = run;
+          while (bits) {
+            const uint32_t bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            ublk[run++] = (uint16_t)(wb + 32 * wi + bit);
+          }
+        }
+        nU += (int32_t)__shfl_sync(0xffffffffu, incl, 31);
+        __syncwarp();
+        for (int r0 = 0; r0 < 8; r0 += 2) {
+          int32_t e[2][16];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r0 + rr);
+            const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i0 + r0 + rr) * a.kcap;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int32_t j = (int32_t)lane + 32 * k;
+              e[rr][k] = j < cnt ? __ldg(sel + j) : -1;
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int r = r0 + rr;
+            const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r);
+            const int32_t bt = __shfl_sync(0xffffffffu, bt_l, r);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int32_t j = (int32_t)lane + 32 * k;
+              const int32_t b = e[rr][k];
+              if (j >= cnt || b < 0 || b > bt) continue;
+              const int32_t o = b - wb;
+              if (o < 0 || o >= K4U_WIN) continue;
+              const uint32_t w = (uint32_t)o >> 5;
+              const uint32_t pos = pre[w] + __popc(bm[w] & ((1u << (o & 31)) - 1u));
+              atomicOr(&rbits[r * (K4U_MAXU / 32) + (pos >> 5)], 1u << (pos & 31));
+              if (b == bt) meta[1 + r] = (int32_t)pos;
+            }
+          }
+        }
+        __syncwarp();
+      }
+      if (nU == 0) {  // only after bad input: one fully masked block keeps every role in step
+        if (lane == 0) ublk[0] = 0;
+        nU = 1;
+      }
+      if (lane == 0) meta[0] = nU;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kTblFull + buf));
+    }
+  } else if (warp == 0 || warp == 3) {
+    // --------------------------- TMA producers (K: warp 0, V: warp 3) ---------------------------
+    const bool is_k = warp == 0;
+    const CUtensorMap* map = is_k ? &tmK : &tmV;
+    const int full0 = is_k ? kKFull : kVFull, empty0 = is_k ? kKEmpty : kVEmpty;
+    const uint32_t base0 = sb0 + (is_k ? K4U_K_OFF : K4U_V_OFF);
+    uint32_t uc = 0, kc = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+      const uint32_t buf = uc & 1;
+      if (!warp_wait(kTblFull + buf, (uc >> 1) & 1)) break;
+      const int32_t g = (int32_t)(u / ntiles);
+      const uint8_t* T = tbl(buf);
+      const uint16_t* ublk = reinterpret_cast<const uint16_t*>(T + K4U_TB_UBLK);
+      const int32_t nU = reinterpret_cast<const int32_t*>(T + K4U_TB_META)[0];
+      const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
+      const int64_t row0 = (int64_t)g * a.ctx_cap;
+      for (int32_t c = 0; c < nch; ++c) {
+        const uint32_t slot = kc & 1;
+        bool r = true;
+        if (lane == 0) {
+          if (kc >= 2) r = mbar_wait(bar(empty0 + slot), ((kc >> 1) - 1) & 1, a.wait_ns, abort_flag);
+          if (r) mbar_arrive_expect_tx(bar(full0 + slot), K4U_SLOT);
+        }
+        ok = __shfl_sync(0xffffffffu, r, 0) != 0;
+        if (!ok) break;
+        if (lane < K4U_CB) {
+          const int32_t p = c * K4U_CB + (int32_t)lane;
+          const int32_t b = ublk[p < nU ? p : nU - 1];  // past the union: a valid block, masked
+          tma_load_3d(base0 + slot * K4U_SLOT + lane * 3072, map, bar(full0 + slot), 0,
+                      (int32_t)(row0 + (int64_t)b * 8), 0);
+        }
+        __syncwarp();
+        ++kc;
+      }
+      if (lane == 0) mbar_arrive(bar(kTblEmpty + buf));
+    }
+    // drain: the latest copies into each slot land before the CTA leaves
+    if (lane == 0)
+      for (uint32_t b = 0; b < 2; ++b)
+        if (kc > b) {
+          const uint32_t last = ((kc - 1 - b) & ~1u) + b;
+          mbar_wait(bar(full0 + b), (last >> 1) & 1, kDrainLimitNs);
+        }
+  } else if (warp == 1) {
+    // ------------------------------- MMA issuer -------------------------------
+    if (lane == 0) {
+      const uint32_t id_s = idesc_bf16_f32(128, 128);
+      const uint32_t id_o = idesc_bf16_f32(128, 192) | (1u << 16);  // B (V) is MN-major
+      uint32_t uc = 0, kc = 0;
+      bool ok = true;
+      auto issue_o = [&](uint32_t c, bool first) -> bool {
+        if (!mbar_wait(bar(kPFull), c & 1, a.wait_ns, abort_flag)) return false;
+        if (!mbar_wait(bar(kVFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t vb = sb0 + K4U_V_OFF + (c & 1) * K4U_SLOT;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          tc_mma_ts(tmem + K4U_COL_O, tmem + K4U_COL_P + 8 * ks, smem_desc_mn_sw128(vb + ks * 6144, 1024, 3072),
+                    id_o, (first && ks == 0) ? 0u : 1u);
+        tc_commit(bar(kVEmpty + (c & 1)));
+        tc_commit(bar(kPvDone));
+        return true;
+      };
+      for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
+        const uint32_t buf = uc & 1;
+        if (!mbar_wait(bar(kTblFull + buf), (uc >> 1) & 1, a.wait_ns, abort_flag)) break;
+        const int32_t nU = reinterpret_cast<const int32_t*>(tbl(buf) + K4U_TB_META)[0];
+        const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
+        mbar_arrive(bar(kTblEmpty + buf));
+        if (!mbar_wait(bar(kQFull), uc & 1, a.wait_ns, abort_flag)) break;
+        for (int32_t j = 0; j < nch && ok; ++j) {
+          const uint32_t c = kc + (uint32_t)j;
+          if (!mbar_wait(bar(kKFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag) ||
+              (c >= 1 && !mbar_wait(bar(kSFree), (c - 1) & 1, a.wait_ns, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t kb = sb0 + K4U_K_OFF + (c & 1) * K4U_SLOT;
+#pragma unroll
+          for (int ks = 0; ks < 12; ++ks)
+            tc_mma_ts(tmem + K4U_COL_S, tmem + K4U_COL_Q + 8 * ks,
+                      smem_desc_k_sw128_sbo(kb + (ks >> 2) * 1024 + (ks & 3) * 32, 3072), id_s, ks > 0 ? 1u : 0u);
+          tc_commit(bar(kKEmpty + (c & 1)));
+          tc_commit(bar(kSFull));
+          if (j == nch - 1) tc_commit(bar(kQEmpty));
+          if (j >= 1) {
+            if (j == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag)) {
+              ok = false;
+              break;
+            }
+            if (!issue_o(c - 1, j == 1)) ok = false;
+          }
+        }
+        if (!ok) break;
+        if (nch == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag)) break;
+        if (!issue_o(kc + (uint32_t)nch - 1, nch == 1)) break;
+        kc += (uint32_t)nch;
+      }
+      tc_commit(bar(kFinal));
+      mbar_wait(bar(kFinal), 0, kDrainLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------- softmax + epilogue -------------------------------
+    // Eight warps: warp w serves TMEM lane quarter w & 3 (pairs 32q .. 32q+31) and one
+    // half of every chunk (keys 64 hf .. 64 hf + 63), of O (d 96 hf ..) and of Q.  The two
+    // halves of a pair agree on each chunk's maximum through shared memory (named barrier
+    // 1 over the eight warps), so both scale their P by the same reference.
+    const uint32_t sw = warp - 4;         // 0..7
+    const uint32_t q = warp & 3;          // TMEM lane quarter of this warp
+    const uint32_t hf = sw >> 2;          // which half of the keys, O and Q
+    const uint32_t m = q * 32 + lane;     // this thread's (row, head) pair = its TMEM lane
+    const uint32_t r = m >> 4, h = m & 15;
+    const uint32_t lbase = (q * 32) << 16;
+    const uint32_t tQ = tmem + lbase + K4U_COL_Q + 48 * hf, tO = tmem + lbase + K4U_COL_O + 96 * hf;
+    const uint32_t tS = tmem + lbase + K4U_COL_S + 64 * hf, tP = tmem + lbase + K4U_COL_P + 32 * hf;
+    float* xchg = reinterpret_cast<float*>(smem + K4U_X_OFF);  // [2 parity][2 half][128] maxima, then [2][128] sums
+    const float sl2 = a.scale_log2;
+    constexpr float kLazy = 8.f;  // reference maximum refreshed only past 2^8
+
+    auto write_q = [&](int64_t u) {  // this half of the Q rows of unit u -> tensor memory
+      const int32_t g = (int32_t)(u / ntiles);
+      const int64_t i = (u % ntiles) * 8 + r;
+      const bool valid = i < a.rows;
+      const uint4* src =
+          reinterpret_cast<const uint4*>(a.q + ((i * a.H) + (int64_t)g * 16 + h) * K4U_D + 96 * hf);
+      uint4 x[12];
+#pragma unroll
+      for (int e = 0; e < 12; ++e) x[e] = valid ? __ldg(src + e) : make_uint4(0u, 0u, 0u, 0u);
+      uint32_t v[32];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        v[4 * e] = x[e].x;
+        v[4 * e + 1] = x[e].y;
+        v[4 * e + 2] = x[e].z;
+        v[4 * e + 3] = x[e].w;
+      }
+      tmem_st_32x32b_x32(tQ, v);
+      float w[16];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        w[4 * e] = __uint_as_float(x[8 + e].x);
+        w[4 * e + 1] = __uint_as_float(x[8 + e].y);
+        w[4 * e + 2] = __uint_as_float(x[8 + e].z);
+        w[4 * e + 3] = __uint_as_float(x[8 + e].w);
+      }
+      tmem_st_32x32b_x16(tQ + 32, w);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQFull));
+    };
+
+    // The eight warps meet on named barrier 1; a failed wait only marks the warp `bad`.
+    // Each warp posts (bad || abort) before a barrier and all of them OR the eight posts
+    // after it, so every warp leaves at the same barrier and none is left waiting in one.
+    volatile uint32_t* post = reinterpret_cast<volatile uint32_t*>(smem + K4U_BAR_OFF + 320);  // [2][8]
+    uint32_t xb = 0;
+    bool bad = false;
+    auto sync_stop = [&]() -> bool {
+      if (lane == 0) post[(xb & 1) * 8 + sw] = (bad || *abort_flag) ? 1u : 0u;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const volatile uint32_t* pp = post + (xb & 1) * 8;
+      const bool st = (pp[0] | pp[1] | pp[2] | pp[3] | pp[4] | pp[5] | pp[6] | pp[7]) != 0;
+      ++xb;
+      return st;
+    };
+    auto wait_ok = [&](int b, uint32_t parity) {  // skipped once the warp is bad
+      if (!bad && !warp_wait(b, parity)) bad = true;
+      return !bad;
+    };
+
+    if ((int64_t)blockIdx.x < n_units) write_q(blockIdx.x);
+    uint32_t uc = 0, kc = 0;
+    for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
+      const uint32_t buf = uc & 1;
+      wait_ok(kTblFull + buf, (uc >> 1) & 1);
+      if (sync_stop()) break;
+      const int32_t g = (int32_t)(u / ntiles);
+      const int64_t i = (u % ntiles) * 8 + r;
+      const bool row_ok = i < a.rows;
+      const uint8_t* T = tbl(buf);
+      const uint32_t* rb = reinterpret_cast<const uint32_t*>(T + K4U_TB_RBITS);
+      const uint32_t* rb_me = rb + r * (K4U_MAXU / 32);
+      const uint32_t* rb_w0 = rb + (2 * q) * (K4U_MAXU / 32);  // the warp's two rows
+      const uint32_t* rb_w1 = rb_w0 + (K4U_MAXU / 32);
+      const int32_t* meta = reinterpret_cast<const int32_t*>(T + K4U_TB_META);
+      const int32_t nU = meta[0];
+      const int32_t own = meta[1 + r];
+      const int32_t tlim = (int32_t)((a.pos0 + i) & 7);
+      const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
+      const int64_t hb = i * a.H + (int64_t)g * 16 + h;
+      if (row_ok && a.gate_per_dim) {  // warm L2 for the epilogue's gate half-row
+        const char* gp = reinterpret_cast<const char*>(a.gate + hb * K4U_D + 96 * hf);
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(gp + 128));
+      }
+      float m_run = -INFINITY, l = 0.f;
+      bool stop = false;
+      for (int32_t j = 0; j < nch; ++j) {
+        const uint32_t c = kc + (uint32_t)j;
+        const uint32_t sh = (uint32_t)(j & 1) * 16 + 8 * hf;
+        const uint32_t mh = (rb_me[j >> 1] >> sh) & 0xFFu;                   // my row, my 8 blocks
+        const uint32_t uh = ((rb_w0[j >> 1] | rb_w1[j >> 1]) >> sh) & 0xFFu;  // the warp's rows (uniform)
+        const int32_t ownj = own - j * K4U_CB - 8 * (int32_t)hf;  // own block's slot in my half, if 0..7
+        float s[64];
+        if (wait_ok(kSFull, c & 1)) {
+          tc_fence_after();
+          uint32_t sa[32], sb[32];
+          tmem_ld_32x32b_x32(tS, sa);
+          tmem_ld_32x32b_x32(tS + 32, sb);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kSFree));
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            s[e] = __uint_as_float(sa[e]);
+            s[32 + e] = __uint_as_float(sb[e]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 64; ++e) s[e] = -INFINITY;
+        }
+        // the own block: keys past the row's position are masked (about one chunk per unit)
+        if (__any_sync(0xffffffffu, ownj >= 0 && ownj < 8)) {
+#pragma unroll
+          for (int blk = 0; blk < 8; ++blk)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (blk == ownj && e > tlim) s[blk * 8 + e] = -INFINITY;
+        }
+        // chunk maximum over this pair's member blocks, agreed between the two halves
+        float mx = -INFINITY;
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) {
+          const float b01 = fmaxf(s[blk * 8 + 0], s[blk * 8 + 1]), b23 = fmaxf(s[blk * 8 + 2], s[blk * 8 + 3]);
+          const float b45 = fmaxf(s[blk * 8 + 4], s[blk * 8 + 5]), b67 = fmaxf(s[blk * 8 + 6], s[blk * 8 + 7]);
+          const float bm = fmaxf(fmaxf(b01, b23), fmaxf(b45, b67));
+          mx = ((mh >> blk) & 1u) ? fmaxf(mx, bm) : mx;
+        }
+        float* xm = xchg + (c & 1) * 256;
+        xm[hf * 128 + m] = mx;
+        if (sync_stop()) {
+          stop = true;
+          break;
+        }
+        mx = fmaxf(xm[m], xm[128 + m]);
+        const float mxs = mx * sl2;
+        if (__any_sync(0xffffffffu, mxs > m_run + kLazy)) {
+          const float m_new = fmaxf(m_run, mxs);
+          const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
+          l *= alpha;
+          m_run = m_new;
+          // O holds this unit's earlier chunks: rescale my half once O(c-1) is complete
+          if (j > 0 && wait_ok(kPvDone, (c - 1) & 1)) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 6; ++cc) {  // 16 columns at a time: s[] stays live meanwhile
+              float o[16];
+              tmem_ld_32x32b_x16(tO + 16 * cc, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] *= alpha;
+              tmem_st_32x32b_x16(tO + 16 * cc, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        // P = 2^(scale_log2 * s - m) on member blocks, 0 elsewhere; blocks neither of the
+        // warp's two rows selected are skipped as a whole
+        uint32_t pw[32];
+        float l0 = 0.f, l1 = 0.f;
+        const float negm = -m_run;
+#pragma unroll
+        for (int blk = 0; blk < 8; ++blk) {
+          uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
+          if ((uh >> blk) & 1u) {
+            const float cb = ((mh >> blk) & 1u) ? negm : -INFINITY;
+            float pv[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(fmaf(s[blk * 8 + e], sl2, cb));
+            l0 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+            l1 += (pv[4] + pv[5]) + (pv[6] + pv[7]);
+            w0 = pack_bf16(pv[0], pv[1]);
+            w1 = pack_bf16(pv[2], pv[3]);
+            w2 = pack_bf16(pv[4], pv[5]);
+            w3 = pack_bf16(pv[6], pv[7]);
+          }
+          pw[blk * 4 + 0] = w0;
+          pw[blk * 4 + 1] = w1;
+          pw[blk * 4 + 2] = w2;
+          pw[blk * 4 + 3] = w3;
+        }
+        l += l0 + l1;
+        // the P columns are free once O(c-1) has read them
+        if ((c == 0 || wait_ok(kPvDone, (c - 1) & 1)) && !bad) {
+          tc_fence_after();
+          tmem_st_32x32b_x32(tP, pw);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kPFull));
+        }
+      }
+      if (stop) break;
+      kc += (uint32_t)nch;
+      // the next unit's Q goes in now: its first S overlaps this epilogue
+      const int64_t un = u + gridDim.x;
+      if (un < n_units && wait_ok(kQEmpty, uc & 1)) {
+        tc_fence_after();
+        write_q(un);
+      }
+      // ---- epilogue: O / l, times sigmoid(gate), bf16 ----
+      float* xl = xchg + 512;
+      xl[hf * 128 + m] = l;
+      const uint4* gs = reinterpret_cast<const uint4*>(a.gate + hb * K4U_D + 96 * hf);
+      float gh = 0.f;
+      if (row_ok && !a.gate_per_dim) gh = __bfloat162float(a.gate[hb]);
+      if (sync_stop()) break;
+      const float lt = xl[m] + xl[128 + m];
+      if (!wait_ok(kPvDone, (kc - 1) & 1)) continue;  // caught at the next unit's barrier
+      tc_fence_after();
+      const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
+      const float kLog2e = 1.4426950408889634f;
+#pragma unroll
+      for (int cc = 0; cc < 3; ++cc) {
+        uint4 gv[4];
+        if (row_ok && a.gate_per_dim) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) gv[e] = __ldg(gs + cc * 4 + e);
+        }
+        uint32_t o[32];
+        tmem_ld_32x32b_x32(tO + 32 * cc, o);
+        tmem_ld_wait();
+        if (row_ok) {
+          uint32_t y[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float g0 = gh, g1 = gh;
+            if (a.gate_per_dim) {
+              const uint4 x = gv[e / 4];
+              const uint32_t gw = (e & 3) == 0 ? x.x : (e & 3) == 1 ? x.y : (e & 3) == 2 ? x.z : x.w;
+              const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw));
+              g0 = f.x;
+              g1 = f.y;
+            }
+            const float s0v = __frcp_rn(1.f + fast_exp2(-g0 * kLog2e));
+            const float s1v = __frcp_rn(1.f + fast_exp2(-g1 * kLog2e));
+            y[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv * s0v, __uint_as_float(o[2 * e + 1]) * inv * s1v);
+          }
+          uint4* dst = reinterpret_cast<uint4*>(a.out + hb * K4U_D + 96 * hf + 32 * cc);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kOEmpty));
+      if (row_ok && a.lse && hf == 0) a.lse[hb] = (m_run + __log2f(lt)) * 0.6931471805599453f;
+      if (lane == 0) mbar_arrive(bar(kTblEmpty + buf));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace sgqa

@@ -22,6 +22,7 @@
 #include "k3_topk.cuh"
 #include "k4_attention.cuh"
 #include "k4tc_attention.cuh"
+#include "k4u_attention.cuh"
 
 using namespace sgqa;
 
@@ -331,9 +332,62 @@ cudaError_t launch_k4tc(const K4TArgs& a, const CUtensorMap& tq, const CUtensorM
   return cudaSuccess;
 }
 
+// The union kernel serves prefill when its shape holds: blocks of 8, 16 heads per group,
+// at most 512 selected blocks per row (a unit's union fits its 4,096-entry table) and block
+// indices below 65,536 (16-bit table entries).  SGQA_K4_IMPL=mma|tc|union overrides.
+bool use_k4u(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
+  static const int forced = [] {
+    const char* e = std::getenv("SGQA_K4_IMPL");
+    if (!e) return -1;
+    if (std::strcmp(e, "union") == 0) return 1;
+    if (std::strcmp(e, "mma") == 0 || std::strcmp(e, "tc") == 0) return 0;
+    return -1;
+  }();
+  const bool fits = p.B == 8 && p.Hg == 16 && p.k <= 512 && !dense && T > 0 &&
+                    (q_start + T - 1) / 8 < (int64_t)K4U_MAX_BLOCKS;
+  return fits && forced == 1;
+}
+
+cudaError_t launch_k4u(const K4UArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k4u_sparse_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K4U_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int64_t n_units = (int64_t)a.G * cdiv(a.rows, 8);
+  const int64_t grid = std::min<int64_t>(n_units, num_sms());
+  if (grid <= 0) return cudaSuccess;
+  k4u_sparse_attn<<<(unsigned)grid, K4U_THREADS, K4U_SMEM, st>>>(a, tk, tv);
+  return cudaGetLastError();
+}
+
 sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void* v, int64_t ctx_cap, const void* gate,
                           const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T, int64_t q_start, void* out,
                           float* lse, int32_t dense, cudaStream_t st) {
+  if (use_k4u(p, dense, T, q_start)) {
+    K4UArgs a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.gate = static_cast<const __nv_bfloat16*>(gate);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.rows = T;
+    a.pos0 = q_start;
+    a.ctx_cap = ctx_cap;
+    a.G = p.G;
+    a.H = p.H;
+    a.kcap = p.k;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.gate_per_dim = p.gate_per_dim;
+    a.wait_ns = g_wait_ns;
+    CUtensorMap tk, tv;
+    const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
+    if (!make_kv_map(&tk, k, rowsz) || !make_kv_map(&tv, v, rowsz)) return SGQA_ERR_CUDA;
+    SGQA_CUDA_OK(launch_k4u(a, tk, tv, st));
+    return SGQA_OK;
+  }
   if (use_k4tc(p)) {
     K4TArgs a{};
     a.gate = static_cast<const __nv_bfloat16*>(gate);
@@ -435,6 +489,14 @@ const char* sgqa_status_string(sgqa_status s) {
 }
 
 int32_t sgqa_abi_version(void) { return SGQA_ABI_VERSION; }
+
+int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode) {
+  Prm p;
+  if (check_params(prm, p) != SGQA_OK || T < 0 || q_start < 0) return -1;
+  if (use_k4u(p, dense_mode, T, q_start)) return SGQA_ATTN_TC_UNION;
+  if (use_k4tc(p)) return SGQA_ATTN_TC_ROW;
+  return SGQA_ATTN_WARP;
+}
 
 sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns) {
   g_wait_ns = ns;

@@ -43,8 +43,9 @@ SGQA_OP_INDEX_TOPK, SGQA_OP_PREFILL, SGQA_OP_DECODE, SGQA_OP_ATTN = 1, 2, 3, 4
 EXPORTS = (
     "sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
     "sgqa_workspace_bytes", "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout",
-    "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc",
+    "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc", "sgqa_attention_kernel",
 )
+ATTN_WARP, ATTN_TC_ROW, ATTN_TC_UNION = 0, 1, 2
 
 
 class SgqaError(RuntimeError):
@@ -79,6 +80,8 @@ _lib.sgqa_status_string.restype = ctypes.c_char_p
 _lib.sgqa_status_string.argtypes = [ctypes.c_int]
 _lib.sgqa_abi_version.restype = ctypes.c_int32
 _lib.sgqa_abi_version.argtypes = []
+_lib.sgqa_attention_kernel.restype = ctypes.c_int32
+_lib.sgqa_attention_kernel.argtypes = [_PP, _I64, _I64, ctypes.c_int32]
 _lib.sgqa_build_block_index.argtypes = [_PP, _P, _I64, _I64, _I64, _P, _I64, _P]
 _lib.sgqa_index_topk.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.sgqa_index_topk_noalloc.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P]
@@ -127,6 +130,11 @@ BF16, I32, F32 = torch.bfloat16, torch.int32, torch.float32
 
 def abi_version() -> int:
     return int(_lib.sgqa_abi_version())
+
+
+def sgqa_attention_kernel(prm: Params, T: int, q_start: int = 0, dense_mode: bool = False) -> int:
+    """Which attention kernel a call with these arguments launches (ATTN_*); -1 if invalid."""
+    return int(_lib.sgqa_attention_kernel(ctypes.byref(prm), T, q_start, 1 if dense_mode else 0))
 
 
 def sgqa_workspace_bytes(prm: Params, op: int, T: int, ctx_len: int, batch: int = 1) -> int:

@@ -229,6 +229,19 @@ SGQA_API sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns);
  * this checks the library's own failure handling. */
 SGQA_API sgqa_status sgqa_selftest_wait_timeout(uint64_t limit_ns, sgqa_stream_t stream);
 
+/* Which attention kernel sgqa_sparse_attn_fwd / sgqa_prefill launch for these arguments
+ * (no launch, no device access): SGQA_ATTN_WARP = one warp per (row, group) on warp-level
+ * MMAs; SGQA_ATTN_TC_ROW = one (row, group) per CTA on tcgen05, keys as the MMA's M (opt-in,
+ * environment SGQA_K4_IMPL=tc); SGQA_ATTN_TC_UNION = 8 query rows per unit over the union of
+ * their selected blocks on tcgen05 (blocks of 8, 16 heads per group, top_k_blocks <= 512,
+ * block indices below 65,536, not dense_mode).  SGQA_K4_IMPL=mma|tc|union, read once per
+ * process, overrides the choice where the arguments allow it.  Returns -1 for invalid
+ * parameters. */
+#define SGQA_ATTN_WARP 0
+#define SGQA_ATTN_TC_ROW 1
+#define SGQA_ATTN_TC_UNION 2
+SGQA_API int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode);
+
 /* Short English description of a status code (static storage). */
 SGQA_API const char* sgqa_status_string(sgqa_status s);
 
