@@ -37,10 +37,13 @@ sys.path.insert(0, ROOT)
 METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline per stage"
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
-# DRAM bytes (read + write) per K4 launch from an ncu capture of the current kernel
-# (profiles/k4_sparse_attn_l128k_tail.md): 6.83 GB for the 65,536 (row, group) units of
-# the l128k_tail workload, scaled to the full 128K launch by kept blocks (x7.875).
-K4_TRAFFIC = {"l128k_tail": 6.833e9, "l128k": 53.8e9}
+# DRAM bytes (read + write) per attention launch from ncu captures of the current kernels
+# on the l128k_tail workload (65,536 (row, group) units), scaled to the full 128K launch by
+# kept blocks (x7.875): the union kernel (profiles/k4u_sparse_attn_l128k_tail.md) 23.59 GB,
+# the warp-level kernel (profiles/k4_sparse_attn_l128k_tail.md) 6.83 GB.
+K4_KERNEL = {0: "k4_sparse_attn", 1: "k4tc_sparse_attn", 2: "k4u_sparse_attn"}
+K4_TRAFFIC = {"k4u_sparse_attn": {"l128k_tail": 23.59e9, "l128k": 185.8e9},
+              "k4_sparse_attn": {"l128k_tail": 6.833e9, "l128k": 53.8e9}}
 K4_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, l128k_tail capture (scaled for l128k)"
 
 
@@ -340,15 +343,17 @@ def run_sgqa(args, rank, world, local_rank):
     stages["k2k3_index_topk"]["k2_tflop"] = round(w["k2_flop"] / 1e12, 4)
     layer_roof = sum(roof.values())
 
+    k4_kernel = K4_KERNEL.get(sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start), "k4_sparse_attn")
+    k4_traffic = K4_TRAFFIC.get(k4_kernel, {}).get(wl.name)
     roofline = {
-        "kernel": "k4_sparse_attn",
+        "kernel": k4_kernel,
         "bound": "hbm",
         "achieved": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9, 1),
         "peak": hbm,
         "unit": "GB/s",
         "frac": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9 / hbm, 4),
-        "traffic": K4_TRAFFIC.get(wl.name),
-        "traffic_source": K4_TRAFFIC_SOURCE if wl.name in K4_TRAFFIC else None,
+        "traffic": k4_traffic,
+        "traffic_source": K4_TRAFFIC_SOURCE if k4_traffic is not None else None,
         "bytes_per_launch": w["k4_bytes"],
         "peak_source": peak_src,
     }

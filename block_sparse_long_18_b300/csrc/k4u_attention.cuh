@@ -51,10 +51,11 @@ constexpr uint32_t K4U_V_OFF = 2 * K4U_SLOT;
 constexpr uint32_t K4U_T_OFF = 4 * K4U_SLOT;
 constexpr uint32_t K4U_BM_OFF = K4U_T_OFF + 2 * K4U_TB;      // uint32 [K4U_WIN / 32] window bitmap
 constexpr uint32_t K4U_PRE_OFF = K4U_BM_OFF + K4U_WIN / 8;   // uint32 [K4U_WIN / 32] prefix counts
-constexpr uint32_t K4U_X_OFF = K4U_PRE_OFF + K4U_WIN / 8;    // float [3][256]: chunk maxima (2 parities), row sums
-constexpr uint32_t K4U_BAR_OFF = K4U_X_OFF + 3 * 256 * 4;
+constexpr uint32_t K4U_X_OFF = K4U_PRE_OFF + K4U_WIN / 8;    // float [128]: row sums per (row, head) pair
+constexpr uint32_t K4U_BAR_OFF = K4U_X_OFF + 128 * 4;
 constexpr uint32_t K4U_SMEM = K4U_BAR_OFF + 512 + 1024;     // + barriers, flags, alignment
 constexpr int K4U_THREADS = 384;
+constexpr uint32_t kSuspendNs = 20000;  // a waiting role sleeps in its polls (woken when the phase completes)
 constexpr uint32_t K4U_COL_Q = 0, K4U_COL_O = 96, K4U_COL_S = 288, K4U_COL_P = 416;
 static_assert(K4U_SMEM <= 232448, "k4u shared memory");
 
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
   // lane 0 waits, the warp agrees on the outcome
   auto warp_wait = [&](int b, uint32_t parity) -> bool {
     bool r = true;
-    if (lane == 0) r = mbar_wait(bar(b), parity, a.wait_ns, abort_flag);
+    if (lane == 0) r = mbar_wait(bar(b), parity, a.wait_ns, abort_flag, kSuspendNs);
     return __shfl_sync(0xffffffffu, r, 0) != 0;
   };
 
@@ -268,6 +269,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     const CUtensorMap* map = is_k ? &tmK : &tmV;
     const int full0 = is_k ? kKFull : kVFull, empty0 = is_k ? kKEmpty : kVEmpty;
     const uint32_t base0 = sb0 + (is_k ? K4U_K_OFF : K4U_V_OFF);
+    // Each union block is fetched once per unit, but neighbouring units (the CTAs in flight
+    // work on adjacent rows of one group) select many of the same blocks: keep K/V in L2.
+    const uint64_t keep = make_l2_evict_last();
     uint32_t uc = 0, kc = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
@@ -283,7 +287,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         const uint32_t slot = kc & 1;
         bool r = true;
         if (lane == 0) {
-          if (kc >= 2) r = mbar_wait(bar(empty0 + slot), ((kc >> 1) - 1) & 1, a.wait_ns, abort_flag);
+          if (kc >= 2) r = mbar_wait(bar(empty0 + slot), ((kc >> 1) - 1) & 1, a.wait_ns, abort_flag, kSuspendNs);
           if (r) mbar_arrive_expect_tx(bar(full0 + slot), K4U_SLOT);
         }
         ok = __shfl_sync(0xffffffffu, r, 0) != 0;
@@ -291,8 +295,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         if (lane < K4U_CB) {
           const int32_t p = c * K4U_CB + (int32_t)lane;
           const int32_t b = ublk[p < nU ? p : nU - 1];  // past the union: a valid block, masked
-          tma_load_3d(base0 + slot * K4U_SLOT + lane * 3072, map, bar(full0 + slot), 0,
-                      (int32_t)(row0 + (int64_t)b * 8), 0);
+          tma_load_3d_hint(base0 + slot * K4U_SLOT + lane * 3072, map, bar(full0 + slot), 0,
+                           (int32_t)(row0 + (int64_t)b * 8), 0, keep);
         }
         __syncwarp();
         ++kc;
@@ -314,8 +318,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       uint32_t uc = 0, kc = 0;
       bool ok = true;
       auto issue_o = [&](uint32_t c, bool first) -> bool {
-        if (!mbar_wait(bar(kPFull), c & 1, a.wait_ns, abort_flag)) return false;
-        if (!mbar_wait(bar(kVFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag)) return false;
+        if (!mbar_wait(bar(kPFull), c & 1, a.wait_ns, abort_flag, kSuspendNs)) return false;
+        if (!mbar_wait(bar(kVFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) return false;
         tc_fence_after();
         const uint32_t vb = sb0 + K4U_V_OFF + (c & 1) * K4U_SLOT;
 #pragma unroll
@@ -328,15 +332,15 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       };
       for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const uint32_t buf = uc & 1;
-        if (!mbar_wait(bar(kTblFull + buf), (uc >> 1) & 1, a.wait_ns, abort_flag)) break;
+        if (!mbar_wait(bar(kTblFull + buf), (uc >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) break;
         const int32_t nU = reinterpret_cast<const int32_t*>(tbl(buf) + K4U_TB_META)[0];
         const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
         mbar_arrive(bar(kTblEmpty + buf));
-        if (!mbar_wait(bar(kQFull), uc & 1, a.wait_ns, abort_flag)) break;
+        if (!mbar_wait(bar(kQFull), uc & 1, a.wait_ns, abort_flag, kSuspendNs)) break;
         for (int32_t j = 0; j < nch && ok; ++j) {
           const uint32_t c = kc + (uint32_t)j;
-          if (!mbar_wait(bar(kKFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag) ||
-              (c >= 1 && !mbar_wait(bar(kSFree), (c - 1) & 1, a.wait_ns, abort_flag))) {
+          if (!mbar_wait(bar(kKFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs) ||
+              (c >= 1 && !mbar_wait(bar(kSFree), (c - 1) & 1, a.wait_ns, abort_flag, kSuspendNs))) {
             ok = false;
             break;
           }
@@ -350,7 +354,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
           tc_commit(bar(kSFull));
           if (j == nch - 1) tc_commit(bar(kQEmpty));
           if (j >= 1) {
-            if (j == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag)) {
+            if (j == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) {
               ok = false;
               break;
             }
@@ -358,7 +362,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
           }
         }
         if (!ok) break;
-        if (nch == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag)) break;
+        if (nch == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) break;
         if (!issue_o(kc + (uint32_t)nch - 1, nch == 1)) break;
         kc += (uint32_t)nch;
       }
@@ -368,19 +372,23 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------- softmax + epilogue -------------------------------
-    // Eight warps: warp w serves TMEM lane quarter w & 3 (pairs 32q .. 32q+31) and one
-    // half of every chunk (keys 64 hf .. 64 hf + 63), of O (d 96 hf ..) and of Q.  The two
-    // halves of a pair agree on each chunk's maximum through shared memory (named barrier
-    // 1 over the eight warps), so both scale their P by the same reference.
+    // Eight warps, two per TMEM lane quarter q = w & 3.  In the chunk loop warp (q, hf) owns
+    // query row 2q + hf, its 16 lanes read through the .16x256b shape: every softmax
+    // decision (which blocks the row selected, the maxima, the rescale) is uniform over the
+    // warp and needs no exchange with other warps.  For Q and the epilogue the two warps of
+    // a quarter split the columns instead (thread = pair, .32x32b).
     const uint32_t sw = warp - 4;         // 0..7
     const uint32_t q = warp & 3;          // TMEM lane quarter of this warp
-    const uint32_t hf = sw >> 2;          // which half of the keys, O and Q
+    const uint32_t hf = sw >> 2;          // row within the quarter; half of Q and O columns
     const uint32_t m = q * 32 + lane;     // this thread's (row, head) pair = its TMEM lane
     const uint32_t r = m >> 4, h = m & 15;
     const uint32_t lbase = (q * 32) << 16;
     const uint32_t tQ = tmem + lbase + K4U_COL_Q + 48 * hf, tO = tmem + lbase + K4U_COL_O + 96 * hf;
-    const uint32_t tS = tmem + lbase + K4U_COL_S + 64 * hf, tP = tmem + lbase + K4U_COL_P + 32 * hf;
-    float* xchg = reinterpret_cast<float*>(smem + K4U_X_OFF);  // [2 parity][2 half][128] maxima, then [2][128] sums
+    const uint32_t rr = 2 * q + hf;        // the query row this warp serves in the chunk loop
+    const uint32_t hA = lane >> 2, hB = hA + 8, kq = 2 * (lane & 3);
+    const uint32_t lb16 = (q * 32 + 16 * hf) << 16;  // the row's 16 TMEM lanes
+    const uint32_t tS16 = tmem + lb16 + K4U_COL_S, tP16 = tmem + lb16 + K4U_COL_P, tO16 = tmem + lb16 + K4U_COL_O;
+    float* xchg = reinterpret_cast<float*>(smem + K4U_X_OFF);  // row sums per pair, for the epilogue
     const float sl2 = a.scale_log2;
     constexpr float kLazy = 8.f;  // reference maximum refreshed only past 2^8
 
@@ -447,13 +455,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       const bool row_ok = i < a.rows;
       const uint8_t* T = tbl(buf);
       const uint32_t* rb = reinterpret_cast<const uint32_t*>(T + K4U_TB_RBITS);
-      const uint32_t* rb_me = rb + r * (K4U_MAXU / 32);
-      const uint32_t* rb_w0 = rb + (2 * q) * (K4U_MAXU / 32);  // the warp's two rows
-      const uint32_t* rb_w1 = rb_w0 + (K4U_MAXU / 32);
       const int32_t* meta = reinterpret_cast<const int32_t*>(T + K4U_TB_META);
       const int32_t nU = meta[0];
-      const int32_t own = meta[1 + r];
-      const int32_t tlim = (int32_t)((a.pos0 + i) & 7);
       const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
       const int64_t hb = i * a.H + (int64_t)g * 16 + h;
       if (row_ok && a.gate_per_dim) {  // warm L2 for the epilogue's gate half-row
@@ -461,115 +464,130 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(gp + 128));
       }
-      float m_run = -INFINITY, l = 0.f;
-      bool stop = false;
+      // chunk loop: this warp serves query row rr of the unit (TMEM lanes 16 rr .. 16 rr + 15);
+      // thread t holds heads hA = t/4 and hB = hA + 8, keys kq, kq + 1 of every block
+      const uint32_t* rb_row = rb + rr * (K4U_MAXU / 32);
+      const int64_t ir = (u % ntiles) * 8 + rr;
+      const int32_t own_r = meta[1 + rr];
+      const int32_t tlim_r = (int32_t)((a.pos0 + ir) & 7);
+      float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
       for (int32_t j = 0; j < nch; ++j) {
         const uint32_t c = kc + (uint32_t)j;
-        const uint32_t sh = (uint32_t)(j & 1) * 16 + 8 * hf;
-        const uint32_t mh = (rb_me[j >> 1] >> sh) & 0xFFu;                   // my row, my 8 blocks
-        const uint32_t uh = ((rb_w0[j >> 1] | rb_w1[j >> 1]) >> sh) & 0xFFu;  // the warp's rows (uniform)
-        const int32_t ownj = own - j * K4U_CB - 8 * (int32_t)hf;  // own block's slot in my half, if 0..7
+        const uint32_t mine = (rb_row[j >> 1] >> ((uint32_t)(j & 1) * 16)) & 0xFFFFu;  // warp-uniform
+        const int32_t ownj = own_r - j * K4U_CB;  // own block's slot in this chunk, if 0..15
         float s[64];
         if (wait_ok(kSFull, c & 1)) {
           tc_fence_after();
-          uint32_t sa[32], sb[32];
-          tmem_ld_32x32b_x32(tS, sa);
-          tmem_ld_32x32b_x32(tS + 32, sb);
+          uint32_t v0[32], v1[32];
+          tmem_ld_16x256b_x8(tS16, v0);
+          tmem_ld_16x256b_x8(tS16 + 64, v1);
           tmem_ld_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kSFree));
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            s[e] = __uint_as_float(sa[e]);
-            s[32 + e] = __uint_as_float(sb[e]);
+            s[e] = __uint_as_float(v0[e]);
+            s[32 + e] = __uint_as_float(v1[e]);
           }
         } else {
 #pragma unroll
           for (int e = 0; e < 64; ++e) s[e] = -INFINITY;
         }
-        // the own block: keys past the row's position are masked (about one chunk per unit)
-        if (__any_sync(0xffffffffu, ownj >= 0 && ownj < 8)) {
+        if (ownj >= 0 && ownj < K4U_CB) {  // the own block: keys past the row's position
 #pragma unroll
-          for (int blk = 0; blk < 8; ++blk)
+          for (int k = 0; k < K4U_CB; ++k)
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (blk == ownj && e > tlim) s[blk * 8 + e] = -INFINITY;
+            for (int e = 0; e < 4; ++e)
+              if (k == ownj && (int32_t)(kq + (e & 1)) > tlim_r) s[4 * k + e] = -INFINITY;
         }
-        // chunk maximum over this pair's member blocks, agreed between the two halves
-        float mx = -INFINITY;
+        // P = 2^(scale_log2 * s - m) on the row's blocks with the current references; the
+        // first pass also finds the chunk's maxima, and a reference more than 2^8 too low
+        // sends the chunk through a second pass after the rescale
+        uint32_t pw[32];
+        float lca = 0.f, lcb = 0.f, xa = -INFINITY, xb = -INFINITY;
+        auto ppass = [&](bool track) {
+          lca = 0.f;
+          lcb = 0.f;
 #pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          const float b01 = fmaxf(s[blk * 8 + 0], s[blk * 8 + 1]), b23 = fmaxf(s[blk * 8 + 2], s[blk * 8 + 3]);
-          const float b45 = fmaxf(s[blk * 8 + 4], s[blk * 8 + 5]), b67 = fmaxf(s[blk * 8 + 6], s[blk * 8 + 7]);
-          const float bm = fmaxf(fmaxf(b01, b23), fmaxf(b45, b67));
-          mx = ((mh >> blk) & 1u) ? fmaxf(mx, bm) : mx;
-        }
-        float* xm = xchg + (c & 1) * 256;
-        xm[hf * 128 + m] = mx;
-        if (sync_stop()) {
-          stop = true;
-          break;
-        }
-        mx = fmaxf(xm[m], xm[128 + m]);
-        const float mxs = mx * sl2;
-        if (__any_sync(0xffffffffu, mxs > m_run + kLazy)) {
-          const float m_new = fmaxf(m_run, mxs);
-          const float alpha = m_new == -INFINITY ? 1.f : fast_exp2(m_run - m_new);
-          l *= alpha;
-          m_run = m_new;
-          // O holds this unit's earlier chunks: rescale my half once O(c-1) is complete
+          for (int k = 0; k < K4U_CB; ++k) {
+            uint32_t w0 = 0u, w1 = 0u;
+            if ((mine >> k) & 1u) {
+              const float x0 = s[4 * k], x1 = s[4 * k + 1], x2 = s[4 * k + 2], x3 = s[4 * k + 3];
+              if (track) {
+                xa = fmaxf(xa, fmaxf(x0, x1));
+                xb = fmaxf(xb, fmaxf(x2, x3));
+              }
+              const float p0 = fast_exp2(fmaf(x0, sl2, -ma)), p1 = fast_exp2(fmaf(x1, sl2, -ma));
+              const float p2 = fast_exp2(fmaf(x2, sl2, -mb)), p3 = fast_exp2(fmaf(x3, sl2, -mb));
+              lca += p0 + p1;
+              lcb += p2 + p3;
+              w0 = pack_bf16(p0, p1);
+              w1 = pack_bf16(p2, p3);
+            }
+            pw[2 * k] = w0;
+            pw[2 * k + 1] = w1;
+          }
+        };
+        ppass(true);
+        if (__any_sync(0xffffffffu, xa * sl2 > ma + kLazy || xb * sl2 > mb + kLazy)) {
+#pragma unroll
+          for (int o = 1; o <= 2; o <<= 1) {
+            xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
+            xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, o));
+          }
+          const float na = fmaxf(ma, xa * sl2), nb = fmaxf(mb, xb * sl2);
+          const float alpha_a = na == -INFINITY ? 1.f : fast_exp2(ma - na);
+          const float alpha_b = nb == -INFINITY ? 1.f : fast_exp2(mb - nb);
+          la *= alpha_a;
+          lb *= alpha_b;
+          ma = na;
+          mb = nb;
+          // O holds this unit's earlier chunks: rescale the row once O(c-1) is complete
           if (j > 0 && wait_ok(kPvDone, (c - 1) & 1)) {
             tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < 6; ++cc) {  // 16 columns at a time: s[] stays live meanwhile
-              float o[16];
-              tmem_ld_32x32b_x16(tO + 16 * cc, o);
+            for (int cc = 0; cc < 6; ++cc) {
+              uint32_t o[16];
+              tmem_ld_16x256b_x4(tO16 + 32 * cc, o);
               tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] *= alpha;
-              tmem_st_32x32b_x16(tO + 16 * cc, o);
+              for (int e = 0; e < 16; ++e)
+                o[e] = __float_as_uint(__uint_as_float(o[e]) * ((e & 2) ? alpha_b : alpha_a));
+              tmem_st_16x256b_x4(tO16 + 32 * cc, o);
             }
             tmem_st_wait();
           }
+          ppass(false);
         }
-        // P = 2^(scale_log2 * s - m) on member blocks, 0 elsewhere; blocks neither of the
-        // warp's two rows selected are skipped as a whole
-        uint32_t pw[32];
-        float l0 = 0.f, l1 = 0.f;
-        const float negm = -m_run;
-#pragma unroll
-        for (int blk = 0; blk < 8; ++blk) {
-          uint32_t w0 = 0u, w1 = 0u, w2 = 0u, w3 = 0u;
-          if ((uh >> blk) & 1u) {
-            const float cb = ((mh >> blk) & 1u) ? negm : -INFINITY;
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) pv[e] = fast_exp2(fmaf(s[blk * 8 + e], sl2, cb));
-            l0 += (pv[0] + pv[1]) + (pv[2] + pv[3]);
-            l1 += (pv[4] + pv[5]) + (pv[6] + pv[7]);
-            w0 = pack_bf16(pv[0], pv[1]);
-            w1 = pack_bf16(pv[2], pv[3]);
-            w2 = pack_bf16(pv[4], pv[5]);
-            w3 = pack_bf16(pv[6], pv[7]);
-          }
-          pw[blk * 4 + 0] = w0;
-          pw[blk * 4 + 1] = w1;
-          pw[blk * 4 + 2] = w2;
-          pw[blk * 4 + 3] = w3;
-        }
-        l += l0 + l1;
+        la += lca;
+        lb += lcb;
         // the P columns are free once O(c-1) has read them
         if ((c == 0 || wait_ok(kPvDone, (c - 1) & 1)) && !bad) {
           tc_fence_after();
-          tmem_st_32x32b_x32(tP, pw);
+          tmem_st_16x128b_x16(tP16, pw);
           tmem_st_wait();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kPFull));
         }
       }
-      if (stop) break;
+      // row sums of the two heads over the quad; the quad leader publishes them (and the lse)
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        la += __shfl_xor_sync(0xffffffffu, la, o);
+        lb += __shfl_xor_sync(0xffffffffu, lb, o);
+      }
+      float* xl = xchg;
+      if ((lane & 3) == 0) {
+        xl[16 * rr + hA] = la;
+        xl[16 * rr + hB] = lb;
+        if (ir < a.rows && a.lse) {
+          const int64_t hr = ir * a.H + (int64_t)g * 16;
+          a.lse[hr + hA] = (ma + __log2f(la)) * 0.6931471805599453f;
+          a.lse[hr + hB] = (mb + __log2f(lb)) * 0.6931471805599453f;
+        }
+      }
       kc += (uint32_t)nch;
       // the next unit's Q goes in now: its first S overlaps this epilogue
       const int64_t un = u + gridDim.x;
@@ -577,14 +595,12 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         tc_fence_after();
         write_q(un);
       }
-      // ---- epilogue: O / l, times sigmoid(gate), bf16 ----
-      float* xl = xchg + 512;
-      xl[hf * 128 + m] = l;
+      // ---- epilogue: O / l, times sigmoid(gate), bf16 (thread = pair m, 96 columns) ----
       const uint4* gs = reinterpret_cast<const uint4*>(a.gate + hb * K4U_D + 96 * hf);
       float gh = 0.f;
       if (row_ok && !a.gate_per_dim) gh = __bfloat162float(a.gate[hb]);
       if (sync_stop()) break;
-      const float lt = xl[m] + xl[128 + m];
+      const float lt = xl[m];
       if (!wait_ok(kPvDone, (kc - 1) & 1)) continue;  // caught at the next unit's barrier
       tc_fence_after();
       const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
@@ -623,7 +639,6 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kOEmpty));
-      if (row_ok && a.lse && hf == 0) a.lse[hb] = (m_run + __log2f(lt)) * 0.6931471805599453f;
       if (lane == 0) mbar_arrive(bar(kTblEmpty + buf));
     }
   }

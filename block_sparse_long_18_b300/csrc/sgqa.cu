@@ -332,9 +332,10 @@ cudaError_t launch_k4tc(const K4TArgs& a, const CUtensorMap& tq, const CUtensorM
   return cudaSuccess;
 }
 
-// The union kernel serves prefill when its shape holds: blocks of 8, 16 heads per group,
-// at most 512 selected blocks per row (a unit's union fits its 4,096-entry table) and block
-// indices below 65,536 (16-bit table entries).  SGQA_K4_IMPL=mma|tc|union overrides.
+// The union kernel serves prefill by default when its shape holds: blocks of 8, 16 heads
+// per group, at most 512 selected blocks per row (a unit's union fits its 4,096-entry
+// table), block indices below 65,536 (16-bit table entries), not dense mode.  Otherwise
+// the warp-level kernel runs.  SGQA_K4_IMPL=mma|tc|union overrides.
 bool use_k4u(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
   static const int forced = [] {
     const char* e = std::getenv("SGQA_K4_IMPL");
@@ -345,7 +346,7 @@ bool use_k4u(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
   }();
   const bool fits = p.B == 8 && p.Hg == 16 && p.k <= 512 && !dense && T > 0 &&
                     (q_start + T - 1) / 8 < (int64_t)K4U_MAX_BLOCKS;
-  return fits && forced == 1;
+  return fits && forced != 0;
 }
 
 cudaError_t launch_k4u(const K4UArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {

@@ -233,10 +233,10 @@ SGQA_API sgqa_status sgqa_selftest_wait_timeout(uint64_t limit_ns, sgqa_stream_t
  * (no launch, no device access): SGQA_ATTN_WARP = one warp per (row, group) on warp-level
  * MMAs; SGQA_ATTN_TC_ROW = one (row, group) per CTA on tcgen05, keys as the MMA's M (opt-in,
  * environment SGQA_K4_IMPL=tc); SGQA_ATTN_TC_UNION = 8 query rows per unit over the union of
- * their selected blocks on tcgen05 (blocks of 8, 16 heads per group, top_k_blocks <= 512,
- * block indices below 65,536, not dense_mode).  SGQA_K4_IMPL=mma|tc|union, read once per
- * process, overrides the choice where the arguments allow it.  Returns -1 for invalid
- * parameters. */
+ * their selected blocks on tcgen05, the default whenever its shape holds (blocks of 8, 16
+ * heads per group, top_k_blocks <= 512, block indices below 65,536, not dense_mode);
+ * SGQA_ATTN_WARP otherwise.  SGQA_K4_IMPL=mma|tc|union, read once per process, overrides
+ * the choice where the arguments allow it.  Returns -1 for invalid parameters. */
 #define SGQA_ATTN_WARP 0
 #define SGQA_ATTN_TC_ROW 1
 #define SGQA_ATTN_TC_UNION 2
