@@ -605,17 +605,25 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       tc_fence_after();
       const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
       const float kLog2e = 1.4426950408889634f;
+      // O leaves tensor memory first, so the next unit's P.V can start while this one gates
+      // and stores
+      uint32_t o0[32], o1[32], o2[32];
+      tmem_ld_32x32b_x32(tO, o0);
+      tmem_ld_32x32b_x32(tO + 32, o1);
+      tmem_ld_32x32b_x32(tO + 64, o2);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kOEmpty));
 #pragma unroll
       for (int cc = 0; cc < 3; ++cc) {
-        uint4 gv[4];
-        if (row_ok && a.gate_per_dim) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) gv[e] = __ldg(gs + cc * 4 + e);
-        }
-        uint32_t o[32];
-        tmem_ld_32x32b_x32(tO + 32 * cc, o);
-        tmem_ld_wait();
+        const uint32_t* o = cc == 0 ? o0 : cc == 1 ? o1 : o2;
         if (row_ok) {
+          uint4 gv[4];
+          if (a.gate_per_dim) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) gv[e] = __ldg(gs + cc * 4 + e);
+          }
           uint32_t y[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
@@ -636,9 +644,6 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
           for (int e = 0; e < 4; ++e) dst[e] = make_uint4(y[4 * e], y[4 * e + 1], y[4 * e + 2], y[4 * e + 3]);
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kOEmpty));
       if (lane == 0) mbar_arrive(bar(kTblEmpty + buf));
     }
   }
