@@ -69,6 +69,14 @@ def _get():
             lib.sgqa_oracle_attention.restype = ctypes.c_int
             lib.sgqa_oracle_attention.argtypes = [ctypes.POINTER(OrcDims), I64, P, P, P, P, P, P, P, I64,
                                                   P, P, ctypes.c_int32, P, P, P]
+            lib.sgqa_oracle_e4m3_to_f64.restype = ctypes.c_double
+            lib.sgqa_oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+            lib.sgqa_oracle_f64_to_e4m3.restype = ctypes.c_uint8
+            lib.sgqa_oracle_f64_to_e4m3.argtypes = [ctypes.c_double]
+            lib.sgqa_oracle_round_e4m3_array.restype = None
+            lib.sgqa_oracle_round_e4m3_array.argtypes = [P, I64, P]
+            lib.sgqa_oracle_block_index_e4m3.restype = ctypes.c_int
+            lib.sgqa_oracle_block_index_e4m3.argtypes = [I64, I64, I64, P, I64, I64, I64, P, I64]
             lib.sgqa_oracle_num_threads.restype = ctypes.c_int
             lib.sgqa_oracle_num_threads.argtypes = []
             _lib = lib
@@ -172,6 +180,45 @@ def block_index(k_proxy, B: int, tok_begin: int, tok_end: int, k_blk=None, nb_ca
     if rc:
         raise ValueError("oracle block_index: bad arguments")
     return k_blk
+
+
+def e4m3_to_f64(codes: np.ndarray) -> np.ndarray:
+    """Exact values of FP8 E4M3 codes (uint8)."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    f = _get().sgqa_oracle_e4m3_to_f64
+    table = np.array([f(i) for i in range(256)], dtype=np.float64)
+    return table[c]
+
+
+def f64_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """One round-to-nearest-even step from double to E4M3 codes, saturating at +-448."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _get().sgqa_oracle_round_e4m3_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def block_index_e4m3(k_proxy, B: int, tok_begin: int, tok_end: int, k_blk=None, nb_cap=None) -> np.ndarray:
+    """The block index of `block_index` stored as FP8 E4M3 codes [G, nb_cap, P] (the decode
+    cache variant; the pages deploy in FP8 but do not describe this cache)."""
+    kp = _u16(k_proxy)
+    G, C, P = kp.shape
+    if nb_cap is None:
+        nb_cap = (C + B - 1) // B
+    if k_blk is None:
+        k_blk = np.zeros((G, nb_cap, P), dtype=np.uint8)
+    k_blk = np.ascontiguousarray(k_blk, dtype=np.uint8)
+    rc = _get().sgqa_oracle_block_index_e4m3(G, P, B, _ptr(kp), C, tok_begin, tok_end, _ptr(k_blk), nb_cap)
+    if rc:
+        raise ValueError("oracle block_index_e4m3: bad arguments")
+    return k_blk
+
+
+def e4m3_as_bf16(codes: np.ndarray) -> np.ndarray:
+    """E4M3 codes re-expressed as bf16 payloads.  Every E4M3 value has at most 4
+    significant bits and an exponent inside bf16's range, so this is exact; it lets
+    `select` score an E4M3 block index unchanged."""
+    return f64_to_bf16(e4m3_to_f64(codes))
 
 
 def select(d: OrcDims, pos, grp, qp_rows, k_blk, want_scores: bool = False):

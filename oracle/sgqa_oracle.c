@@ -117,6 +117,77 @@ int sgqa_oracle_block_index(int64_t G, int64_t P, int64_t B, const uint16_t* k_p
   return 0;
 }
 
+/* ---- FP8 block-proxy cache (decode variant) ----------------------------------------- */
+
+/* The block proxies can be cached as FP8 E4M3 (1 sign bit, 4 exponent bits with bias 7,
+ * 3 mantissa bits; no infinities, code 0x7f/0xff is NaN; largest finite 448 = 1.75 x 2^8,
+ * smallest normal 2^-6, subnormals m x 2^-9 for m = 1..7).  The pages deploy the model in
+ * FP8 (ai.info article, "Why StepFun chose 92 transformer blocks"); storing the block
+ * index this way is a variant of R1, not a step the pages describe. */
+
+/* Exact value of an E4M3 code. */
+double sgqa_oracle_e4m3_to_f64(uint8_t c) {
+  const int s = c >> 7, E = (c >> 3) & 15, M = c & 7;
+  if (E == 15 && M == 7) return NAN;
+  double v = E == 0 ? ldexp((double)M, -9) : ldexp(1.0 + M / 8.0, E - 7);
+  return s ? -v : v;
+}
+
+/* One rounding step from double to E4M3: to nearest, ties to even, finite values beyond
+ * the largest code saturating to +-448.  Same construction as the bf16 rounding above:
+ * count quanta of x's binade (2^-9 below the normal range), round the count with
+ * nearbyint (half to even), then encode the exactly representable result. */
+uint8_t sgqa_oracle_f64_to_e4m3(double x) {
+  if (isnan(x)) return (uint8_t)0x7f;
+  const uint8_t sign = signbit(x) ? (uint8_t)0x80 : (uint8_t)0;
+  const double a = fabs(x);
+  if (a == 0.0) return sign;
+  int e;
+  (void)frexp(a, &e); /* a in [2^(e-1), 2^e) */
+  int lead = e - 1;
+  if (lead < -6) lead = -6;
+  const double quantum = ldexp(1.0, lead - 3);
+  double r = nearbyint(a / quantum) * quantum;
+  if (r > 448.0) r = 448.0;
+  if (r == 0.0) return sign;
+  if (r < ldexp(1.0, -6)) return (uint8_t)(sign | (uint8_t)(r / ldexp(1.0, -9))); /* subnormal */
+  int er;
+  (void)frexp(r, &er); /* r in [2^(er-1), 2^er) */
+  const int E = er - 1 + 7;
+  const int M = (int)((r / ldexp(1.0, er - 1) - 1.0) * 8.0);
+  return (uint8_t)(sign | (uint8_t)(E << 3) | (uint8_t)M);
+}
+
+void sgqa_oracle_round_e4m3_array(const double* x, int64_t n, uint8_t* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = sgqa_oracle_f64_to_e4m3(x[i]);
+}
+
+/* O1 with an E4M3 cache: the same fp64 block mean, rounded once to E4M3. */
+int sgqa_oracle_block_index_e4m3(int64_t G, int64_t P, int64_t B, const uint16_t* k_proxy,
+                                 int64_t ctx_cap, int64_t tok_begin, int64_t tok_end,
+                                 uint8_t* k_blk, int64_t nb_cap) {
+  if (G <= 0 || P <= 0 || B <= 0 || tok_begin < 0 || tok_end < tok_begin || tok_end > ctx_cap)
+    return 1;
+  if (tok_end == tok_begin) return 0;
+  int64_t b0 = tok_begin / B;
+  int64_t b1 = (tok_end + B - 1) / B;
+  if (b1 > nb_cap) return 1;
+  for (int64_t g = 0; g < G; ++g) {
+#pragma omp parallel for schedule(static)
+    for (int64_t b = b0; b < b1; ++b) {
+      int64_t first = b * B;
+      int64_t n = tok_end - first < B ? tok_end - first : B;
+      for (int64_t p = 0; p < P; ++p) {
+        double sum = 0.0;
+        for (int64_t j = 0; j < n; ++j)
+          sum += sgqa_oracle_bf16_to_f64(k_proxy[(g * ctx_cap + first + j) * P + p]);
+        k_blk[(g * nb_cap + b) * P + p] = sgqa_oracle_f64_to_e4m3(sum / (double)n);
+      }
+    }
+  }
+  return 0;
+}
+
 /* ---- O2 + O3: indexer scores and top-k selection (R2, R3, R4) ----------------------- */
 
 typedef struct {

@@ -309,10 +309,12 @@ def test_chunk1m_sampled_rows(sg):
     torch.cuda.empty_cache()
 
 
-def test_coverage_from_lse_matches_oracle_coverage(sg):
-    """The coverage diagnostic: exp(LSE_sel - LSE_dense) from the GPU equals the oracle's
-    dense-softmax mass on the selected tokens, computed from scratch."""
-    wl = gen.small_workload(T=600, G=2, Hg=16, B=8, k=12, planted=True)
+@pytest.mark.parametrize("B,k", [(8, 12), (1, 96), (2, 48), (4, 24), (16, 6)])
+def test_coverage_from_lse_matches_oracle_coverage(sg, B, k):
+    """The coverage diagnostic (and its sweep over block sizes at one token budget):
+    exp(LSE_sel - LSE_dense) from the GPU equals the oracle's dense-softmax mass on the
+    selected tokens, computed from scratch."""
+    wl = gen.small_workload(T=600, G=2, Hg=16, B=B, k=k, planted=True)
     inp = _to_cuda(gen.make_inputs(wl, seed=12))
     prm = _prm(sg, wl)
     res = _gpu_prefill(sg, inp, wl, prm)
@@ -333,4 +335,4 @@ def test_coverage_from_lse_matches_oracle_coverage(sg):
         _, _, cov = oracle.attention(d, rows, grp, u16(inp.q[:, hs]), u16(inp.gate[:, hs]), u16(inp.k), u16(inp.v),
                                      sel, cnt, want_coverage=True)
         np.testing.assert_allclose(cov_gpu[:, hs], cov, atol=3e-3, rtol=0)
-        assert np.all(cov[: 8 * (wl.k - 1)] > 1 - 1e-12)  # rows whose every block is kept
+        assert np.all(cov[: wl.B * (wl.k - 1)] > 1 - 1e-12)  # rows whose every block is kept

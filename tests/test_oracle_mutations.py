@@ -22,6 +22,10 @@ MUTATIONS = {
     "keeps_one_block_too_few": [("int64_t take = bt < d->k - 1 ? bt : d->k - 1;",
                                  "int64_t take = bt < d->k - 2 ? bt : (d->k > 2 ? d->k - 2 : 0);")],
     "softmax_no_max_shift_wrong_lse": [("if (lse) lse[r * Hg + h] = m + log(l);", "if (lse) lse[r * Hg + h] = log(l);")],
+    "e4m3_exponent_bias": [("ldexp(1.0 + M / 8.0, E - 7)", "ldexp(1.0 + M / 8.0, E - 8)")],
+    "e4m3_round_down": [("double r = nearbyint(a / quantum) * quantum;", "double r = floor(a / quantum) * quantum;")],
+    "e4m3_no_subnormal_floor": [("if (lead < -6) lead = -6;", "if (lead < -9) lead = -9;")],
+    "e4m3_no_saturation": [("if (r > 448.0) r = 448.0;", "if (r > 480.0) r = 480.0;")],
 }
 
 PIN_CALLS = [
@@ -35,6 +39,10 @@ PIN_CALLS = [
     lambda: pins.test_attention_two_token_worked_example(),
     lambda: pins.test_attention_sparse_selection_is_a_subset_softmax(),
     lambda: pins.test_coverage_closed_forms(),
+    lambda: pins.test_e4m3_decoding_matches_torch(),
+    lambda: pins.test_e4m3_rounding_matches_torch_on_float32_values(),
+    lambda: pins.test_e4m3_saturation_and_special_values(),
+    lambda: pins.test_e4m3_cache_of_integer_proxy_means(),
 ]
 
 

@@ -88,6 +88,70 @@ def _rne_fraction_bf16(fr: Fraction) -> float:
 
 
 # ---------------------------------------------------------------------------------------
+# FP8 E4M3 (the decode block-proxy cache variant)
+# ---------------------------------------------------------------------------------------
+
+def _e4m3_torch_values():
+    return torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decoding_matches_torch():
+    """Every one of the 256 codes decodes to torch's float8_e4m3fn value (a library routine)."""
+    ours = oracle.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    ref = _e4m3_torch_values()
+    assert np.array_equal(np.isnan(ours), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(ours[ok], ref[ok])
+    assert np.all(np.signbit(ours[ok]) == np.signbit(ref[ok]))
+
+
+def test_e4m3_rounding_matches_torch_on_float32_values():
+    """Round to nearest even below saturation equals torch's conversion: random values,
+    every midpoint between adjacent codes (ties) and points just beside them, subnormals."""
+    rng = np.random.default_rng(21)
+    table = _e4m3_torch_values()
+    pos = np.unique(table[(~np.isnan(table)) & (table >= 0)])            # 0 .. 448
+    mids = (pos[1:] + pos[:-1]) / 2
+    near = np.concatenate([np.nextafter(mids.astype(np.float32), np.float32(0)),
+                           np.nextafter(mids.astype(np.float32), np.float32(1e9))]).astype(np.float64)
+    x = np.concatenate([rng.standard_normal(50_000) * 3.0, rng.uniform(-464, 464, 20_000),
+                        rng.uniform(-2 ** -6, 2 ** -6, 5_000), mids, -mids, near, -near, pos, -pos])
+    x = x.astype(np.float32)
+    x = x[np.abs(x) <= 464].astype(np.float64)
+    ours = oracle.f64_to_e4m3(x)
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_saturation_and_special_values():
+    """Finite values past the largest code (448) saturate (the conversion the GPU uses), NaN
+    stays NaN, signed zero keeps its sign, and the first value that rounds up from the
+    largest subnormal (7 x 2^-9) lands on the smallest normal 2^-6."""
+    big = np.array([465.0, 500.0, 1e6, -470.0, -1e30])
+    assert oracle.f64_to_e4m3(big).tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]
+    assert oracle.f64_to_e4m3(np.array([np.nan])).tolist() == [0x7F]
+    assert oracle.f64_to_e4m3(np.array([0.0, -0.0])).tolist() == [0x00, 0x80]
+    assert oracle.e4m3_to_f64(oracle.f64_to_e4m3(np.array([7.5 * 2.0 ** -9]))).tolist() == [2.0 ** -6]
+
+
+def test_e4m3_cache_of_integer_proxy_means():
+    """Integer proxies in [-4, 4] average to multiples of 1/8 over a full block of 8; the
+    E4M3 cache holds their round-to-nearest-even values, and its bf16 re-expression is exact
+    (so the bf16 scoring path of the oracle scores the E4M3 cache unchanged)."""
+    rng = np.random.default_rng(22)
+    G, C, P, B = 2, 64, 64, 8
+    kp_i = rng.integers(-4, 5, size=(G, C, P))
+    kp = _bits(torch.from_numpy(kp_i.astype(np.float32)).to(torch.bfloat16))
+    codes = oracle.block_index_e4m3(kp, B, 0, C)
+    means = kp_i.reshape(G, C // B, B, P).sum(axis=2) / 8.0                 # exact
+    ref = torch.from_numpy(means.astype(np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes, ref)
+    assert np.array_equal(oracle.bf16_to_f64(oracle.e4m3_as_bf16(codes)), oracle.e4m3_to_f64(codes))
+    # the quantisation is visible: 17/8 = 2.125 is a tie between 2 and 2.25 and goes to 2
+    assert oracle.e4m3_to_f64(oracle.f64_to_e4m3(np.array([2.125]))).tolist() == [2.0]
+
+
+# ---------------------------------------------------------------------------------------
 # O1: block index
 # ---------------------------------------------------------------------------------------
 
