@@ -448,7 +448,8 @@ def run_sgqa(args, rank, world, local_rank):
 # decode step timing (not the headline metric; reported for the decode workload)
 # ---------------------------------------------------------------------------------------
 
-def run_decode(args, local_rank):
+def run_decode(args, local_rank, fp8=False):
+    """Decode step latency; with fp8 the block-proxy cache is FP8 E4M3 (sgqa_decode_fp8)."""
     from block_sparse_long_18_b300 import build as _build
 
     _build.build()
@@ -462,9 +463,11 @@ def run_decode(args, local_rank):
     prm = sgqa.params(G=wl.G, Hg=wl.Hg, D=wl.D, P=wl.P, B=wl.B, k=wl.k)
     total = inp.k.shape[1]
     batch = len(inp.ctx_len)
-    k_blk = torch.zeros((wl.G, total // wl.B, wl.P), dtype=torch.bfloat16, device=dev)
+    k_blk = torch.zeros((wl.G, total // wl.B, wl.P), dtype=torch.uint8 if fp8 else torch.bfloat16, device=dev)
+    build_idx = sgqa.sgqa_build_block_index_fp8 if fp8 else sgqa.sgqa_build_block_index
+    decode = sgqa.sgqa_decode_fp8 if fp8 else sgqa.sgqa_decode
     for L, off in zip(inp.ctx_len, inp.kv_off):
-        sgqa.sgqa_build_block_index(prm, inp.k_proxy, off, off + L - 1, k_blk)
+        build_idx(prm, inp.k_proxy, off, off + L - 1, k_blk)
     sel = torch.empty((wl.G, batch, wl.k), dtype=torch.int32, device=dev)
     cnt = torch.empty((wl.G, batch), dtype=torch.int32, device=dev)
     out = torch.empty((batch, wl.H, wl.D), dtype=torch.bfloat16, device=dev)
@@ -474,8 +477,8 @@ def run_decode(args, local_rank):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
-        sgqa.sgqa_decode(prm, inp.ctx_len, inp.kv_off, inp.q, inp.q_proxy, inp.gate, inp.k, inp.v, inp.k_proxy,
-                         k_blk, sel, cnt, out, lse, ws)
+        decode(prm, inp.ctx_len, inp.kv_off, inp.q, inp.q_proxy, inp.gate, inp.k, inp.v, inp.k_proxy,
+               k_blk, sel, cnt, out, lse, ws)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -492,15 +495,17 @@ def run_decode(args, local_rank):
         raise RuntimeError("device error in decode")
     ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
     nb = sum((L - 1) // wl.B for L in inp.ctx_len)           # blocks scored per group
-    idx_bytes = wl.G * nb * wl.P * 2
+    idx_bytes = wl.G * nb * wl.P * (1 if fp8 else 2)
     gather = wl.G * sum(min(wl.k, (L - 1) // wl.B + 1) for L in inp.ctx_len) * wl.B * wl.D * 2 * 2
     hbm, _, _, src = load_peaks()
     return {
         "metric": "Sparse GQA decode step latency (8 sequences, 256K-1M context)",
         "value": round(ms, 4), "unit": "ms/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "tokens_per_s": round(batch / (ms / 1e3), 1), "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"decode: {batch} sequences, ctx_len {inp.ctx_len}, G={wl.G} x Hg={wl.Hg}, D={wl.D}, "
-                               f"P={wl.P}, block {wl.B}, top-k {wl.k}",
+        "warmup": args.warmup, "tokens_per_s": round(batch / (ms / 1e3), 1),
+        "dtype": "bf16 (block-proxy cache e4m3)" if fp8 else "bf16", "data": "synthetic",
+        "config": {"workload": f"decode{'_fp8' if fp8 else ''}: {batch} sequences, ctx_len {inp.ctx_len}, "
+                               f"G={wl.G} x Hg={wl.Hg}, D={wl.D}, P={wl.P}, block {wl.B}, top-k {wl.k}"
+                               + (", block-proxy cache FP8 E4M3" if fp8 else ""),
                    "l2": "flushed before every step"},
         "roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + gather + 4 * wl.G * nb * 2,
                      "roofline_ms": round((idx_bytes + gather + 8 * wl.G * nb) / (hbm * 1e9) * 1e3, 4),
@@ -561,7 +566,7 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["sgqa", "reference"], default="sgqa")
-    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "l128k_b1", "chunk1m", "l128k_tail", "decode"])
+    ap.add_argument("--workload", default="l128k", choices=["tiny", "l32k", "l128k", "l128k_b1", "chunk1m", "l128k_tail", "decode", "decode_fp8"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-coverage", action="store_true")
@@ -577,9 +582,9 @@ def main():
             return 0
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return 0
-    if args.workload == "decode":
+    if args.workload in ("decode", "decode_fp8"):
         if rank == 0:
-            print(json.dumps(run_decode(args, local_rank)), flush=True)
+            print(json.dumps(run_decode(args, local_rank, fp8=args.workload == "decode_fp8")), flush=True)
         return 0
     if world > 1:
         torch.cuda.set_device(local_rank)

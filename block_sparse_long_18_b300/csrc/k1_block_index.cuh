@@ -10,14 +10,20 @@
 // 512-byte token rows (P = 256) and writes a whole 512-byte block row.  The sum runs in
 // fp32 in token order; full blocks multiply by 1/B (exact, B is a power of two), partial
 // blocks divide in double so that the result is rounded to bf16 only once.
+//
+// The decode cache can hold the block index as FP8 E4M3 instead (the pages deploy the model
+// in FP8; this cache is a variant): the same fp32 sum, rounded once to E4M3 (to nearest,
+// ties to even, saturating at +-448) by the hardware conversion -- from fp32 for full
+// blocks (x 1/B is exact) and from fp64 for partial ones.
 #pragma once
+#include <cuda_fp8.h>
 #include "ptx.cuh"
 
 namespace sgqa {
 
 struct K1Args {
   const __nv_bfloat16* k_proxy;
-  __nv_bfloat16* k_blk;
+  void* k_blk;          // bf16 or E4M3 codes, [G, nb_cap, P]
   int64_t ctx_cap, nb_cap;
   int64_t tok_end;      // tokens present
   int64_t blk_begin;    // first block to build
@@ -27,10 +33,48 @@ struct K1Args {
   const int64_t* seq_tok_end;  // device or nullptr
 };
 
+// The 8 means of one thread, stored as bf16 (16 bytes) or E4M3 (8 bytes) at element `e0`
+// of the block row.
+template <bool E4M3>
+__device__ __forceinline__ void k1_store(void* row, int pv, const float (&acc)[8], int64_t n, int B) {
+  const float inv_b = 1.0f / (float)B;
+  if (!E4M3) {
+    uint4 o;
+    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+    if (n == B) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) op[e] = pack_bf16(acc[2 * e] * inv_b, acc[2 * e + 1] * inv_b);
+    } else {
+      const double dn = (double)n;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        __nv_bfloat16 lo = __double2bfloat16((double)acc[2 * e] / dn);
+        __nv_bfloat16 hi = __double2bfloat16((double)acc[2 * e + 1] / dn);
+        op[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
+      }
+    }
+    reinterpret_cast<uint4*>(row)[pv] = o;
+  } else {
+    uint8_t c[8];
+    if (n == B) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = __nv_cvt_float_to_fp8(acc[e] * inv_b, __NV_SATFINITE, __NV_E4M3);
+    } else {
+      const double dn = (double)n;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = __nv_cvt_double_to_fp8((double)acc[e] / dn, __NV_SATFINITE, __NV_E4M3);
+    }
+    uint2 o;
+    o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 8) | ((uint32_t)c[2] << 16) | ((uint32_t)c[3] << 24);
+    o.y = (uint32_t)c[4] | ((uint32_t)c[5] << 8) | ((uint32_t)c[6] << 16) | ((uint32_t)c[7] << 24);
+    reinterpret_cast<uint2*>(row)[pv] = o;
+  }
+}
+
+template <bool E4M3>
 __global__ void __launch_bounds__(256) k1_block_index(K1Args a) {
   const int vec_per_row = a.P / 8;
   const int64_t n_vec = (int64_t)a.G * a.n_blocks * vec_per_row;
-  const float inv_b = 1.0f / (float)a.B;
   for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += (int64_t)gridDim.x * blockDim.x) {
     const int pv = (int)(v % vec_per_row);
     const int64_t gb = v / vec_per_row;
@@ -59,38 +103,26 @@ __global__ void __launch_bounds__(256) k1_block_index(K1Args a) {
         acc[2 * e + 1] += f.y;
       }
     }
-    uint4 o;
-    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-    if (n == a.B) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) op[e] = pack_bf16(acc[2 * e] * inv_b, acc[2 * e + 1] * inv_b);
-    } else {
-      const double dn = (double)n;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat16 lo = __double2bfloat16((double)acc[2 * e] / dn);
-        __nv_bfloat16 hi = __double2bfloat16((double)acc[2 * e + 1] / dn);
-        op[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-      }
-    }
-    reinterpret_cast<uint4*>(a.k_blk + (g * a.nb_cap + b) * a.P)[pv] = o;
+    const int64_t row = (g * a.nb_cap + b) * a.P;
+    k1_store<E4M3>(E4M3 ? (void*)(static_cast<uint8_t*>(a.k_blk) + row) : (void*)(static_cast<__nv_bfloat16*>(a.k_blk) + row),
+                   pv, acc, n, a.B);
   }
 }
 
 // Decode form: for each sequence s rebuild the block holding its newest token.
 struct K1SeqArgs {
   const __nv_bfloat16* k_proxy;  // [G, total, P]
-  __nv_bfloat16* k_blk;          // [G, total / B, P]
+  void* k_blk;                   // [G, total / B, P], bf16 or E4M3 codes
   int64_t total;
   int32_t G, P, B, batch;
   int64_t ctx_len[256];
   int64_t kv_off[256];
 };
 
+template <bool E4M3>
 __global__ void __launch_bounds__(256) k1_block_index_seq(const __grid_constant__ K1SeqArgs a) {
   const int vec_per_row = a.P / 8;
   const int n_vec = a.G * a.batch * vec_per_row;
-  const float inv_b = 1.0f / (float)a.B;
   const int64_t nb_total = a.total / a.B;
   for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < n_vec; v += gridDim.x * blockDim.x) {
     const int pv = v % vec_per_row;
@@ -120,21 +152,9 @@ __global__ void __launch_bounds__(256) k1_block_index_seq(const __grid_constant_
         acc[2 * e + 1] += f.y;
       }
     }
-    uint4 o;
-    uint32_t* op = reinterpret_cast<uint32_t*>(&o);
-    if (n == a.B) {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) op[e] = pack_bf16(acc[2 * e] * inv_b, acc[2 * e + 1] * inv_b);
-    } else {
-      const double dn = (double)n;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat16 lo = __double2bfloat16((double)acc[2 * e] / dn);
-        __nv_bfloat16 hi = __double2bfloat16((double)acc[2 * e + 1] / dn);
-        op[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-      }
-    }
-    reinterpret_cast<uint4*>(a.k_blk + ((int64_t)g * nb_total + a.kv_off[s] / a.B + bl) * a.P)[pv] = o;
+    const int64_t row = ((int64_t)g * nb_total + a.kv_off[s] / a.B + bl) * a.P;
+    k1_store<E4M3>(E4M3 ? (void*)(static_cast<uint8_t*>(a.k_blk) + row) : (void*)(static_cast<__nv_bfloat16*>(a.k_blk) + row),
+                   pv, acc, n, a.B);
   }
 }
 

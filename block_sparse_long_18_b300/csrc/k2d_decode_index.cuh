@@ -5,13 +5,15 @@
 // from HBM: one warp reads one 512-byte block row per load (P = 256), eight rows per step
 // with the next step's eight already in flight.
 #pragma once
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include "ptx.cuh"
 
 namespace sgqa {
 
 struct K2dArgs {
   const __nv_bfloat16* qp;    // [G, batch, P]
-  const __nv_bfloat16* kblk;  // [G, nb_total, P]
+  const void* kblk;           // [G, nb_total, P], bf16 (k2d_decode_index) or E4M3 codes (_e4m3)
   float* scores;              // [G, batch, ld]
   int64_t ld, nb_total;
   int32_t G, P, B, batch;
@@ -39,7 +41,8 @@ __global__ void __launch_bounds__(256) k2d_decode_index(const __grid_constant__ 
       qv[2 * e + 1] = f.y;
     }
   }
-  const __nv_bfloat16* base = a.kblk + ((int64_t)g * a.nb_total + a.kv_off[s] / a.B) * a.P;
+  const __nv_bfloat16* base =
+      static_cast<const __nv_bfloat16*>(a.kblk) + ((int64_t)g * a.nb_total + a.kv_off[s] / a.B) * a.P;
   float* out = a.scores + (int64_t)gs * a.ld;
   const int64_t b_lo = (int64_t)blockIdx.x * a.rows_per_cta;
   int64_t b_hi = b_lo + a.rows_per_cta;
@@ -83,6 +86,84 @@ __global__ void __launch_bounds__(256) k2d_decode_index(const __grid_constant__ 
 #pragma unroll
       for (int r = 1; r < RW; ++r) v = lane == r ? acc[r] : v;
       out[b0 + lane] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < RW; ++r) cur[r] = nxt[r];
+  }
+}
+
+// The same scores from an E4M3 block-proxy cache: half the bytes of the bf16 cache.  A lane
+// reads 16 codes (16 bytes) of a row, P / 16 lanes cover a row and a warp load covers
+// 32 / (P / 16) rows; eight loads per step with the next step's eight in flight.  Codes are
+// widened exactly (E4M3 -> f16 -> f32) and the dot product runs in fp32.
+__global__ void __launch_bounds__(256) k2d_decode_index_e4m3(const __grid_constant__ K2dArgs a) {
+  const int gs = blockIdx.y;  // g * batch + s
+  const int g = gs / a.batch, s = gs % a.batch;
+  const int64_t n = (a.ctx_len[s] - 1) / a.B;  // candidates 0 .. b_t - 1
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int lpr = a.P / 16;      // lanes per row: 4, 8 or 16
+  const int rpl = 32 / lpr;      // rows per warp load
+  const int sub = lane % lpr, rsub = lane / lpr;
+  float qv[16];
+  {
+    const uint4* qs = reinterpret_cast<const uint4*>(a.qp + ((int64_t)g * a.batch + s) * a.P + 16 * sub);
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      const uint4 w = __ldg(qs + hlf);
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(h[e]);
+        qv[8 * hlf + 2 * e] = f.x;
+        qv[8 * hlf + 2 * e + 1] = f.y;
+      }
+    }
+  }
+  const uint8_t* base =
+      static_cast<const uint8_t*>(a.kblk) + ((int64_t)g * a.nb_total + a.kv_off[s] / a.B) * a.P + 16 * sub;
+  float* out = a.scores + (int64_t)gs * a.ld;
+  const int64_t b_lo = (int64_t)blockIdx.x * a.rows_per_cta;
+  int64_t b_hi = b_lo + a.rows_per_cta;
+  if (b_hi > n) b_hi = n;
+  constexpr int RW = 8;
+  const int64_t wrows = (int64_t)RW * rpl;  // rows of one warp step
+  auto load = [&](int64_t b0, uint4 (&w)[RW]) {
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      const int64_t b = b0 + r * rpl + rsub;
+      w[r] = b < b_hi ? __ldg(reinterpret_cast<const uint4*>(base + b * a.P)) : make_uint4(0, 0, 0, 0);
+    }
+  };
+  const int64_t step = 8 * wrows;  // 8 warps
+  uint4 cur[RW], nxt[RW];
+  int64_t b0 = b_lo + warp * wrows;
+  if (b0 < b_hi) load(b0, cur);
+  for (; b0 < b_hi; b0 += step) {
+    if (b0 + step < b_hi) load(b0 + step, nxt);
+    float acc[RW];
+#pragma unroll
+    for (int r = 0; r < RW; ++r) {
+      const uint16_t* c2 = reinterpret_cast<const uint16_t*>(&cur[r]);
+      float sum = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const __half2 hv = __half2(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2[e], __NV_E4M3));
+        const float2 f = __half22float2(hv);
+        sum = fmaf(qv[2 * e], f.x, sum);
+        sum = fmaf(qv[2 * e + 1], f.y, sum);
+      }
+      acc[r] = sum;
+    }
+    for (int o = lpr / 2; o > 0; o >>= 1) {
+#pragma unroll
+      for (int r = 0; r < RW; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+    }
+    if (sub == 0) {
+#pragma unroll
+      for (int r = 0; r < RW; ++r) {
+        const int64_t b = b0 + r * rpl + rsub;
+        if (b < b_hi) out[b] = acc[r];
+      }
     }
 #pragma unroll
     for (int r = 0; r < RW; ++r) cur[r] = nxt[r];

@@ -218,11 +218,14 @@ cudaError_t launch_k3(K3Args a, int64_t max_cand, uint8_t* ws, const IndexWs& ws
   return cudaGetLastError();
 }
 
-cudaError_t launch_k1(const K1Args& a, cudaStream_t st) {
+cudaError_t launch_k1(const K1Args& a, cudaStream_t st, bool e4m3 = false) {
   const int64_t n_vec = (int64_t)a.G * a.n_blocks * (a.P / 8);
   if (n_vec <= 0) return cudaSuccess;
   const int64_t grid = std::min<int64_t>(cdiv(n_vec, 256), (int64_t)num_sms() * 16);
-  k1_block_index<<<(unsigned)grid, 256, 0, st>>>(a);
+  if (e4m3)
+    k1_block_index<true><<<(unsigned)grid, 256, 0, st>>>(a);
+  else
+    k1_block_index<false><<<(unsigned)grid, 256, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -541,8 +544,8 @@ size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64
   return 0;
 }
 
-sgqa_status sgqa_build_block_index(const sgqa_params* prm, const void* k_proxy, int64_t ctx_cap, int64_t tok_begin,
-                                   int64_t tok_end, void* k_blk, int64_t nb_cap, sgqa_stream_t stream) {
+static sgqa_status build_block_index(const sgqa_params* prm, const void* k_proxy, int64_t ctx_cap, int64_t tok_begin,
+                                     int64_t tok_end, void* k_blk, int64_t nb_cap, sgqa_stream_t stream, bool e4m3) {
   Prm p;
   sgqa_status s = check_params(prm, p);
   if (s != SGQA_OK) return s;
@@ -554,7 +557,7 @@ sgqa_status sgqa_build_block_index(const sgqa_params* prm, const void* k_proxy, 
   if (b1 > nb_cap) return SGQA_ERR_INVALID_ARGUMENT;
   K1Args a{};
   a.k_proxy = static_cast<const __nv_bfloat16*>(k_proxy);
-  a.k_blk = static_cast<__nv_bfloat16*>(k_blk);
+  a.k_blk = k_blk;
   a.ctx_cap = ctx_cap;
   a.nb_cap = nb_cap;
   a.tok_end = tok_end;
@@ -563,8 +566,19 @@ sgqa_status sgqa_build_block_index(const sgqa_params* prm, const void* k_proxy, 
   a.G = p.G;
   a.P = p.P;
   a.B = p.B;
-  SGQA_CUDA_OK(launch_k1(a, reinterpret_cast<cudaStream_t>(stream)));
+  SGQA_CUDA_OK(launch_k1(a, reinterpret_cast<cudaStream_t>(stream), e4m3));
   return SGQA_OK;
+}
+
+sgqa_status sgqa_build_block_index(const sgqa_params* prm, const void* k_proxy, int64_t ctx_cap, int64_t tok_begin,
+                                   int64_t tok_end, void* k_blk, int64_t nb_cap, sgqa_stream_t stream) {
+  return build_block_index(prm, k_proxy, ctx_cap, tok_begin, tok_end, k_blk, nb_cap, stream, false);
+}
+
+sgqa_status sgqa_build_block_index_fp8(const sgqa_params* prm, const void* k_proxy, int64_t ctx_cap,
+                                       int64_t tok_begin, int64_t tok_end, void* k_blk_e4m3, int64_t nb_cap,
+                                       sgqa_stream_t stream) {
+  return build_block_index(prm, k_proxy, ctx_cap, tok_begin, tok_end, k_blk_e4m3, nb_cap, stream, true);
 }
 
 sgqa_status sgqa_index_topk(const sgqa_params* prm, const void* q_proxy, int64_t T, int64_t q_start, const void* k_blk,
@@ -642,10 +656,11 @@ sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, c
   return sgqa_sparse_attn_fwd(prm, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, 0, stream);
 }
 
-sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len, const int64_t* kv_off,
-                        const void* q, const void* q_proxy, const void* gate, const void* k_cache, const void* v_cache,
-                        const void* k_proxy_cache, void* k_blk_cache, int64_t total, int32_t* sel_idx,
-                        int32_t* sel_cnt, void* out, float* lse, void* ws, size_t ws_bytes, sgqa_stream_t stream) {
+static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len, const int64_t* kv_off,
+                              const void* q, const void* q_proxy, const void* gate, const void* k_cache,
+                              const void* v_cache, const void* k_proxy_cache, void* k_blk_cache, int64_t total,
+                              int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse, void* ws, size_t ws_bytes,
+                              sgqa_stream_t stream, bool e4m3) {
   Prm p;
   sgqa_status s = check_params(prm, p);
   if (s != SGQA_OK) return s;
@@ -682,7 +697,7 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
     if (!aligned16(k_proxy_cache)) return SGQA_ERR_INVALID_ARGUMENT;
     K1SeqArgs a1{};
     a1.k_proxy = static_cast<const __nv_bfloat16*>(k_proxy_cache);
-    a1.k_blk = static_cast<__nv_bfloat16*>(k_blk_cache);
+    a1.k_blk = k_blk_cache;
     a1.total = total;
     a1.G = p.G;
     a1.P = p.P;
@@ -693,14 +708,17 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
       a1.kv_off[i] = kv_off[i];
     }
     const int n_vec = p.G * batch * (p.P / 8);
-    k1_block_index_seq<<<(unsigned)cdiv(n_vec, 256), 256, 0, st>>>(a1);
+    if (e4m3)
+      k1_block_index_seq<true><<<(unsigned)cdiv(n_vec, 256), 256, 0, st>>>(a1);
+    else
+      k1_block_index_seq<false><<<(unsigned)cdiv(n_vec, 256), 256, 0, st>>>(a1);
     SGQA_CUDA_OK(cudaGetLastError());
   }
   // 2. indexer scores (matrix-vector per sequence and group)
   if (max_cand > 0) {
     K2dArgs a2{};
     a2.qp = static_cast<const __nv_bfloat16*>(q_proxy);
-    a2.kblk = static_cast<const __nv_bfloat16*>(k_blk_cache);
+    a2.kblk = k_blk_cache;
     a2.scores = scores;
     a2.ld = ld;
     a2.nb_total = nb_total;
@@ -714,7 +732,10 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
       a2.kv_off[i] = kv_off[i];
     }
     dim3 grid((unsigned)cdiv(max_cand, a2.rows_per_cta), (unsigned)(p.G * batch));
-    k2d_decode_index<<<grid, 256, 0, st>>>(a2);
+    if (e4m3)
+      k2d_decode_index_e4m3<<<grid, 256, 0, st>>>(a2);
+    else
+      k2d_decode_index<<<grid, 256, 0, st>>>(a2);
     SGQA_CUDA_OK(cudaGetLastError());
   }
   // 3. top-k
@@ -790,6 +811,23 @@ sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ct
     SGQA_CUDA_OK(cudaGetLastError());
   }
   return SGQA_OK;
+}
+
+sgqa_status sgqa_decode(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len, const int64_t* kv_off,
+                        const void* q, const void* q_proxy, const void* gate, const void* k_cache, const void* v_cache,
+                        const void* k_proxy_cache, void* k_blk_cache, int64_t total, int32_t* sel_idx,
+                        int32_t* sel_cnt, void* out, float* lse, void* ws, size_t ws_bytes, sgqa_stream_t stream) {
+  return run_decode(prm, batch, ctx_len, kv_off, q, q_proxy, gate, k_cache, v_cache, k_proxy_cache, k_blk_cache,
+                    total, sel_idx, sel_cnt, out, lse, ws, ws_bytes, stream, false);
+}
+
+sgqa_status sgqa_decode_fp8(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len, const int64_t* kv_off,
+                            const void* q, const void* q_proxy, const void* gate, const void* k_cache,
+                            const void* v_cache, const void* k_proxy_cache, void* k_blk_cache_e4m3, int64_t total,
+                            int32_t* sel_idx, int32_t* sel_cnt, void* out, float* lse, void* ws, size_t ws_bytes,
+                            sgqa_stream_t stream) {
+  return run_decode(prm, batch, ctx_len, kv_off, q, q_proxy, gate, k_cache, v_cache, k_proxy_cache,
+                    k_blk_cache_e4m3, total, sel_idx, sel_cnt, out, lse, ws, ws_bytes, stream, true);
 }
 
 }  // extern "C"

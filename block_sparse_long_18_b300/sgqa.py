@@ -44,6 +44,7 @@ EXPORTS = (
     "sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
     "sgqa_workspace_bytes", "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout",
     "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc", "sgqa_attention_kernel",
+    "sgqa_build_block_index_fp8", "sgqa_decode_fp8",
 )
 ATTN_WARP, ATTN_TC_ROW, ATTN_TC_UNION = 0, 1, 2
 
@@ -90,6 +91,9 @@ _lib.sgqa_prefill.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P,
                               ctypes.c_size_t, _P]
 _lib.sgqa_decode.argtypes = [_PP, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
                              ctypes.c_size_t, _P]
+_lib.sgqa_decode_fp8.argtypes = [_PP, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
+                             ctypes.c_size_t, _P]
+_lib.sgqa_build_block_index_fp8.argtypes = [_PP, _P, _I64, _I64, _I64, _P, _I64, _P]
 _lib.sgqa_workspace_bytes.restype = ctypes.c_size_t
 _lib.sgqa_workspace_bytes.argtypes = [_PP, ctypes.c_int32, _I64, _I64, ctypes.c_int32]
 _lib.sgqa_get_device_error.argtypes = [_P]
@@ -148,6 +152,14 @@ def sgqa_build_block_index(prm: Params, k_proxy, tok_begin: int, tok_end: int, k
            "sgqa_build_block_index")
 
 
+def sgqa_build_block_index_fp8(prm: Params, k_proxy, tok_begin: int, tok_end: int, k_blk_e4m3, stream=None):
+    """Block index as FP8 E4M3 codes (a uint8 tensor [G, nb_cap, P]) for the decode cache."""
+    G, C, P = k_proxy.shape
+    _check(_lib.sgqa_build_block_index_fp8(ctypes.byref(prm), _dev(k_proxy, BF16, "k_proxy"), C, tok_begin, tok_end,
+                                           _dev(k_blk_e4m3, torch.uint8, "k_blk_e4m3"), k_blk_e4m3.shape[1],
+                                           _stream(stream)), "sgqa_build_block_index_fp8")
+
+
 def sgqa_index_topk(prm: Params, q_proxy, q_start: int, k_blk, sel_idx, sel_cnt, ws, stream=None):
     G, T, P = q_proxy.shape
     _check(_lib.sgqa_index_topk(ctypes.byref(prm), _dev(q_proxy, BF16, "q_proxy"), T, q_start,
@@ -204,6 +216,21 @@ def sgqa_decode(prm: Params, ctx_len, kv_off, q, q_proxy, gate, k_cache, v_cache
                             k_cache.shape[1], _dev(sel_idx, I32, "sel_idx"), _dev(sel_cnt, I32, "sel_cnt"),
                             _dev(out, BF16, "out"), _dev(lse, F32, "lse"), _dev(ws, torch.uint8, "ws"), ws.numel(),
                             _stream(stream)), "sgqa_decode")
+
+
+def sgqa_decode_fp8(prm: Params, ctx_len, kv_off, q, q_proxy, gate, k_cache, v_cache, k_proxy_cache,
+                    k_blk_cache_e4m3, sel_idx, sel_cnt, out, lse, ws, stream=None):
+    """sgqa_decode over an FP8 E4M3 block-proxy cache (uint8 [G, total / B, P])."""
+    batch = len(ctx_len)
+    cl = (ctypes.c_int64 * batch)(*[int(x) for x in ctx_len])
+    ko = (ctypes.c_int64 * batch)(*[int(x) for x in kv_off])
+    _check(_lib.sgqa_decode_fp8(ctypes.byref(prm), batch, cl, ko, _dev(q, BF16, "q"), _dev(q_proxy, BF16, "q_proxy"),
+                                _dev(gate, BF16, "gate"), _dev(k_cache, BF16, "k_cache"),
+                                _dev(v_cache, BF16, "v_cache"), _dev(k_proxy_cache, BF16, "k_proxy_cache"),
+                                _dev(k_blk_cache_e4m3, torch.uint8, "k_blk_cache_e4m3"), k_cache.shape[1],
+                                _dev(sel_idx, I32, "sel_idx"), _dev(sel_cnt, I32, "sel_cnt"), _dev(out, BF16, "out"),
+                                _dev(lse, F32, "lse"), _dev(ws, torch.uint8, "ws"), ws.numel(), _stream(stream)),
+           "sgqa_decode_fp8")
 
 
 def sgqa_get_device_error(stream=None) -> int:

@@ -209,6 +209,29 @@ SGQA_API sgqa_status sgqa_index_topk_noalloc(const sgqa_params* prm, const void*
                                              const void* k_blk, int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt,
                                              sgqa_stream_t stream);
 
+/* ---------------------------------------------------------------------------------
+ * FP8 block-proxy cache (decode variant).  The pages deploy the model in FP8 (ai.info
+ * article, "Why StepFun chose 92 transformer blocks") but do not say how the indexer's
+ * block proxies are stored; these two entries keep them as FP8 E4M3 codes (1 sign, 4
+ * exponent bits with bias 7, 3 mantissa bits; largest finite 448), which halves the
+ * bytes the decode indexer streams.
+ *
+ * sgqa_build_block_index_fp8: as sgqa_build_block_index, but k_blk_e4m3 is uint8 codes
+ *   [G, nb_cap, P]; each block mean (fp32 sum of the bf16 proxies, times 1/B, or divided
+ *   in fp64 for a partial block) is rounded once to E4M3, to nearest, ties to even,
+ *   saturating at +-448.  Base 16-byte aligned.
+ * sgqa_decode_fp8: as sgqa_decode, but k_blk_cache_e4m3 is uint8 codes [G, total / B, P]
+ *   (the rebuilt block is written as E4M3).  Scores widen the codes exactly to fp32.
+ * ------------------------------------------------------------------------------- */
+SGQA_API sgqa_status sgqa_build_block_index_fp8(const sgqa_params* prm, const void* k_proxy, int64_t ctx_cap,
+                                                int64_t tok_begin, int64_t tok_end, void* k_blk_e4m3,
+                                                int64_t nb_cap, sgqa_stream_t stream);
+SGQA_API sgqa_status sgqa_decode_fp8(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len,
+                                     const int64_t* kv_off, const void* q, const void* q_proxy, const void* gate,
+                                     const void* k_cache, const void* v_cache, const void* k_proxy_cache,
+                                     void* k_blk_cache_e4m3, int64_t total, int32_t* sel_idx, int32_t* sel_cnt,
+                                     void* out, float* lse, void* ws, size_t ws_bytes, sgqa_stream_t stream);
+
 /* Workspace bytes needed by `op` for T query rows ending at context length ctx_len
  * (decode: the largest ctx_len of the batch).  Returns 0 for an invalid request. */
 SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64_t ctx_len, int32_t batch);
