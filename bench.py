@@ -39,10 +39,10 @@ HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
 # DRAM bytes (read + write) per attention launch from ncu captures of the current kernels
 # on the l128k_tail workload (65,536 (row, group) units), scaled to the full 128K launch by
-# kept blocks (x7.875): the union kernel (profiles/k4u_sparse_attn_l128k_tail.md) 23.59 GB,
+# kept blocks (x7.875): the union kernel (profiles/k4u_sparse_attn_l128k_tail.md) 23.56 GB,
 # the warp-level kernel (profiles/k4_sparse_attn_l128k_tail.md) 6.83 GB.
 K4_KERNEL = {0: "k4_sparse_attn", 1: "k4tc_sparse_attn", 2: "k4u_sparse_attn"}
-K4_TRAFFIC = {"k4u_sparse_attn": {"l128k_tail": 23.59e9, "l128k": 185.8e9},
+K4_TRAFFIC = {"k4u_sparse_attn": {"l128k_tail": 23.56e9, "l128k": 185.5e9},
               "k4_sparse_attn": {"l128k_tail": 6.833e9, "l128k": 53.8e9}}
 K4_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, l128k_tail capture (scaled for l128k)"
 
