@@ -726,7 +726,7 @@ static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64
     a2.P = p.P;
     a2.B = p.B;
     a2.batch = batch;
-    a2.rows_per_cta = 1024;
+    a2.rows_per_cta = e4m3 ? 2048 : 1024;  // the same bytes per CTA with the 1-byte cache
     for (int i = 0; i < batch; ++i) {
       a2.ctx_len[i] = ctx_len[i];
       a2.kv_off[i] = kv_off[i];

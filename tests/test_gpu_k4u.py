@@ -80,3 +80,39 @@ def test_union_attention_sampled_rows_long_context():
 def test_warp_attention_forced():
     """The warp-level kernel stays reachable (and correct) when forced."""
     _run("mma", 0, UNION_CASES[:3])
+
+
+def test_union_attention_wait_timeout_is_reported_and_recoverable():
+    """Every bounded wait of the union kernel given no time (limit 0): the launch gives up,
+    reports SGQA_ERR_DEVICE_TIMEOUT, drains its copies and MMAs and returns; the next call
+    in the same context reproduces the normal output bit for bit."""
+    code = r"""
+import sys
+sys.path.insert(0, {root!r}); sys.path.insert(0, {tests!r})
+import torch
+from block_sparse_long_18_b300 import build
+build.build()
+from block_sparse_long_18_b300 import inputs as gen, sgqa
+wl = gen.small_workload(T=256, G=2, Hg=16, B=8, k=16, planted=True)
+inp = gen.make_inputs(wl, seed=13, device="cuda")
+prm = sgqa.params(G=wl.G, Hg=wl.Hg, k=wl.k)
+assert sgqa.sgqa_attention_kernel(prm, wl.T) == sgqa.ATTN_TC_UNION
+res = sgqa.prefill(prm, inp.q, inp.k, inp.v, inp.gate, inp.q_proxy, inp.k_proxy)
+torch.cuda.synchronize()
+assert sgqa.sgqa_get_device_error() == 0
+out = torch.empty_like(inp.q)
+sgqa.sgqa_set_wait_timeout_ns(0)
+try:
+    sgqa.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, res.sel_idx, res.sel_cnt, 0, out)
+    err = sgqa.sgqa_get_device_error()
+finally:
+    sgqa.sgqa_set_wait_timeout_ns(1_000_000_000)
+assert err == 5, err
+sgqa.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, res.sel_idx, res.sel_cnt, 0, out)
+assert sgqa.sgqa_get_device_error() == 0
+assert torch.equal(out, res.out)
+print("ok")
+""".format(root=ROOT, tests=HERE)
+    env = dict(os.environ, SGQA_K4_IMPL="union")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-3000:] + r.stderr[-3000:]
