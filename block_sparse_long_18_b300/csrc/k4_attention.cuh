@@ -534,10 +534,11 @@ __global__ void __launch_bounds__(256) k4_combine(const K4CombineArgs a) {
   // O: lane d-slice (d = lane + 32 e), summed over the splits with their weights
   float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   const float* po = a.part_o + (gr * a.nsplit * 16 + h) * K4_D + lane;
+  // no branch on the weight: every split's loads can be in flight together (a split that
+  // got no keys wrote zero partials and has weight 0)
 #pragma unroll 8
   for (int s = 0; s < a.nsplit; ++s) {
     const float w = __shfl_sync(0xffffffffu, ws, s);
-    if (w == 0.f) continue;  // warp-uniform
     const float* ps = po + (int64_t)s * 16 * K4_D;
 #pragma unroll
     for (int e = 0; e < 6; ++e) acc[e] = fmaf(w, __ldg(ps + 32 * e), acc[e]);

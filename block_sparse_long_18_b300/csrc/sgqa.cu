@@ -807,7 +807,7 @@ static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64
     c.nsplit = nsplit;
     c.gate_per_dim = p.gate_per_dim;
     const int64_t warps = (int64_t)p.G * batch * p.Hg;
-    k4_combine<<<(unsigned)cdiv(warps * 32, 256), 256, 0, st>>>(c);
+    k4_combine<<<(unsigned)cdiv(warps * 32, 128), 128, 0, st>>>(c);  // 4 warps per CTA: spread over the SMs
     SGQA_CUDA_OK(cudaGetLastError());
   }
   return SGQA_OK;
