@@ -580,6 +580,11 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
+        if args.workload in ("decode", "decode_fp8"):  # the oracle arm times prefill workloads
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle reference arm times the prefill "
+                                                                  "workloads only; decode has no reference line"}),
+                  flush=True)
+            return 0
         print(json.dumps(run_reference(args, rank, world)), flush=True)
         return 0
     if args.workload in ("decode", "decode_fp8"):
