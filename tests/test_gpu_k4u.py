@@ -54,11 +54,15 @@ UNION_CASES = [
     dict(T=2048, G=1, Hg=16, B=8, k=512),
     dict(T=1000, G=1, Hg=16, B=8, k=1),
 ]
-# Sampled rows: unions near the 4,096-entry capacity (k = 512 far into the context) and
-# the 32K-style planted layout.
+# Sampled rows: unions near the 4,096-entry capacity (k = 512 far into the context), the
+# 32K-style planted layout, several builder windows, and the largest block index served.
 UNION_SAMPLED = [
     dict(T=1024, G=1, Hg=16, B=8, k=512, q_start=60000, planted=True, rows=48),
     dict(T=4096, G=2, Hg=16, B=8, k=512, q_start=8192, planted=True, rows=48),
+    # block indices past one builder window (16,384 blocks): four windows per unit
+    dict(T=256, G=1, Hg=16, B=8, k=512, q_start=400000, planted=True, rows=32),
+    # the last supported block index (65,535): the union tables' 16-bit entries at their limit
+    dict(T=128, G=1, Hg=16, B=8, k=512, q_start=524160, planted=True, rows=32),
 ]
 
 
