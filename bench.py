@@ -37,14 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline per stage"
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
-# DRAM bytes (read + write) per attention launch from ncu captures of the current kernels
-# on the l128k_tail workload (65,536 (row, group) units), scaled to the full 128K launch by
-# kept blocks (x7.875): the union kernel (profiles/k4u_sparse_attn_l128k_tail.md) 23.56 GB,
-# the warp-level kernel (profiles/k4_sparse_attn_l128k_tail.md) 6.83 GB.
-K4_KERNEL = {0: "k4_sparse_attn", 1: "k4tc_sparse_attn", 2: "k4u_sparse_attn"}
-K4_TRAFFIC = {"k4u_sparse_attn": {"l128k_tail": 23.56e9, "l128k": 185.5e9},
-              "k4_sparse_attn": {"l128k_tail": 6.833e9, "l128k": 53.8e9}}
-K4_TRAFFIC_SOURCE = "ncu dram__bytes_read.sum + dram__bytes_write.sum, l128k_tail capture (scaled for l128k)"
+K4_KERNEL = {1: "k4_sparse_attn", 2: "k4u_sparse_attn"}
 
 
 def load_peaks():
@@ -75,10 +68,57 @@ def work_model(wl):
     w["k2_bytes"] = G * P * 2 * (T + (q0 + T) // B) + 4 * G * sum_bt
     w["k3_bytes"] = 4 * G * sum_bt + 4 * G * sum_n
     w["k4_flop"] = 4 * D * H * sum_att
+    # per-(row, group) gathers: every kept block read once per row that keeps it (the
+    # survey's primary K4 line; a kernel that shares gathers across rows moves far less)
     w["k4_gather_bytes"] = 2 * 2 * D * B * G * sum_n
-    w["k4_bytes"] = w["k4_gather_bytes"] + 3 * 2 * T * H * D + 4 * G * sum_n + 4 * G * T + 4 * T * H
+    # bytes every K4 must move: Q, gate and O once, the selection and LSE once, and K/V of
+    # every block some row selected once (set by the caller from the selection, else every
+    # causal block of the context)
+    w["k4_rows_bytes"] = 3 * 2 * T * H * D + 4 * G * sum_n + 4 * G * T + 4 * T * H
+    w["k4_kv_once_bytes"] = 2 * 2 * D * B * G * ((q0 + T + B - 1) // B)
     w["sum_n"] = sum_n
+    w["sum_bt"] = sum_bt
     return w
+
+
+def selection_stats(plan, wl, units_per_pass=4096):
+    """From the step's selection: how many distinct (group, block) pairs some row selected
+    (the K/V every attention kernel must read at least once), and for units of 8 query rows
+    the size of each union and the 128-key chunks the union kernel runs over it."""
+    if wl.T % 8:
+        return None
+    sel = plan.sel_idx  # [G, T, k], ascending, -1 padded
+    G, T, k = sel.shape
+    nb = (wl.q_start + wl.T + wl.B - 1) // wl.B
+    used = torch.zeros((G, nb + 1), dtype=torch.bool, device=sel.device)
+    chunks = 0
+    blocks = 0
+    units = sel.view(G, T // 8, 8 * k)
+    for u0 in range(0, T // 8, units_per_pass):
+        part = units[:, u0:u0 + units_per_pass]
+        srt, _ = torch.sort(part, dim=-1)
+        valid = srt >= 0
+        new = valid.clone()
+        new[..., 1:] &= srt[..., 1:] != srt[..., :-1]
+        nu = new.sum(dim=-1)  # [G, units]
+        blocks += int(nu.sum())
+        chunks += int(((nu + 15) // 16).sum())
+        for g in range(G):
+            used[g].index_fill_(0, (srt[g][valid[g]]).long(), True)
+        del srt, valid, new
+    return {"kv_blocks_selected": int(used.sum()), "union_chunks": chunks,
+            "union_mean_blocks": round(blocks / (G * (T // 8)), 1)}
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
 
 
 # ---------------------------------------------------------------------------------------
@@ -333,35 +373,63 @@ def run_sgqa(args, rank, world, local_rank):
     ms = max_over_ranks(float(step_ms.mean()), world, dev)
     value = job_value(wl.T, world, ms)
 
-    # ---- roofline of each stage ----
+    # ---- roofline of each stage (survey's per-stage line: max of FLOPs at the bf16 peak and
+    # algorithmic bytes at the HBM peak, both measured on the B300s) ----
     w = work_model(wl)
+    sel_stats = selection_stats(plan, wl)
+    if sel_stats is not None:
+        w["k4_kv_once_bytes"] = sel_stats["kv_blocks_selected"] * 2 * 2 * wl.D * wl.B
+    k4_compulsory = w["k4_rows_bytes"] + w["k4_kv_once_bytes"]
     k1_ms, ik_ms, k4_ms = (float(x) for x in stage_ms.mean(axis=0))
-    hbm_bps = hbm * 1e9
+    hbm_bps, tf = hbm * 1e9, bf16 * 1e12
+    k2_scores_bytes = 4 * wl.G * w["sum_bt"]
     roof = {
         "k1_block_index": w["k1_bytes"] / hbm_bps * 1e3,
-        "k2k3_index_topk": max(w["k2_flop"] / (bf16 * 1e12), w["k2_bytes"] / hbm_bps) * 1e3 + w["k3_bytes"] / hbm_bps * 1e3,
-        "k4_sparse_attn": max(w["k4_flop"] / (bf16 * 1e12), w["k4_bytes"] / hbm_bps) * 1e3,
+        "k2k3_index_topk": (max(w["k2_flop"] / tf, w["k2_bytes"] / hbm_bps) + w["k3_bytes"] / hbm_bps) * 1e3,
+        "k4_sparse_attn": max(w["k4_flop"] / tf, k4_compulsory / hbm_bps) * 1e3,
     }
     meas = {"k1_block_index": k1_ms, "k2k3_index_topk": ik_ms, "k4_sparse_attn": k4_ms}
     stages = {kname: {"ms": round(meas[kname], 4), "roofline_ms": round(roof[kname], 4),
                       "frac": round(roof[kname] / meas[kname], 4)} for kname in meas}
-    stages["k4_sparse_attn"]["tensor_tflops"] = round(w["k4_flop"] / (k4_ms / 1e3) / 1e12, 2)
+    stages["k1_block_index"]["bound"] = "hbm"
+    stages["k2k3_index_topk"]["bound"] = "hbm (scores written by the indexer and read by the top-k)"
     stages["k2k3_index_topk"]["k2_tflop"] = round(w["k2_flop"] / 1e12, 4)
+    stages["k2k3_index_topk"]["score_bytes"] = k2_scores_bytes
+    # secondary: scores never leaving the SM (operands, selection out, FLOPs at peak)
+    fused_floor = max(w["k2_flop"] / tf, (w["k2_bytes"] - k2_scores_bytes + 4 * wl.G * w["sum_n"]) / hbm_bps) * 1e3
+    stages["k2k3_index_topk"]["fused_floor_ms"] = round(fused_floor, 4)
+    k4s = stages["k4_sparse_attn"]
+    k4s["bound"] = "tensor" if w["k4_flop"] / tf >= k4_compulsory / hbm_bps else "hbm"
+    k4s["useful_tflop"] = round(w["k4_flop"] / 1e12, 3)
+    k4s["useful_tflops"] = round(w["k4_flop"] / (k4_ms / 1e3) / 1e12, 2)
+    k4s["compulsory_bytes"] = k4_compulsory
+    k4s["frac_vs_sustained_peak"] = (round(max(w["k4_flop"] / (bf16_sus * 1e12), k4_compulsory / hbm_bps) * 1e3
+                                           / k4_ms, 4) if bf16_sus else None)
+    # secondary lines: the per-(row, group) gather bytes (how much the kernel's sharing of
+    # gathers saves) and, for the union kernel, the MMA work it issues including the
+    # (row, head) pairs masked out of a union block
+    k4s["per_row_gather_bytes"] = w["k4_gather_bytes"] + w["k4_rows_bytes"]
+    k4s["per_row_gather_frac_of_hbm"] = round(k4s["per_row_gather_bytes"] / (k4_ms / 1e3) / hbm_bps, 4)
+    k4_kernel = K4_KERNEL.get(sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start), "k4_sparse_attn")
+    if sel_stats is not None and k4_kernel == "k4u_sparse_attn":
+        issued = sel_stats["union_chunks"] * 128 * 128 * wl.D * 4
+        k4s["union_mean_blocks"] = sel_stats["union_mean_blocks"]
+        k4s["issued_mma_tflop"] = round(issued / 1e12, 3)
+        k4s["issued_tflops"] = round(issued / (k4_ms / 1e3) / 1e12, 2)
+        k4s["useful_share_of_issued"] = round(w["k4_flop"] / issued, 4)
     layer_roof = sum(roof.values())
 
-    k4_kernel = K4_KERNEL.get(sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start), "k4_sparse_attn")
-    k4_traffic = K4_TRAFFIC.get(k4_kernel, {}).get(wl.name)
     roofline = {
         "kernel": k4_kernel,
-        "bound": "hbm",
-        "achieved": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9, 1),
-        "peak": hbm,
-        "unit": "GB/s",
-        "frac": round(w["k4_bytes"] / (k4_ms / 1e3) / 1e9 / hbm, 4),
-        "traffic": k4_traffic,
-        "traffic_source": K4_TRAFFIC_SOURCE if k4_traffic is not None else None,
-        "bytes_per_launch": w["k4_bytes"],
-        "peak_source": peak_src,
+        "bound": k4s["bound"],
+        "achieved": k4s["useful_tflops"] if k4s["bound"] == "tensor" else round(k4_compulsory / (k4_ms / 1e3) / 1e9, 1),
+        "peak": bf16 if k4s["bound"] == "tensor" else hbm,
+        "unit": "TFLOP/s" if k4s["bound"] == "tensor" else "GB/s",
+        "frac": k4s["frac"],
+        "traffic": None,
+        "algorithmic": {"useful_flop_per_launch": w["k4_flop"], "compulsory_bytes_per_launch": k4_compulsory},
+        "peak_source": f"{peak_src}: bf16 burst (kernel timed alone by its own events)",
+        "frac_vs_sustained_peak": k4s["frac_vs_sustained_peak"],
     }
 
     # ---- end to end through the public API, from pinned host memory ----
@@ -381,7 +449,8 @@ def run_sgqa(args, rank, world, local_rank):
         e_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in ev])), world, dev)
         e2e = {"value": job_value(wl.T, world, e_ms), "unit": "tokens/s", "ms_per_step": round(e_ms, 3),
                "h2d_bytes_per_step": hp.h2d_bytes(), "d2h_bytes_per_step": hp.d2h_bytes(),
-               "api": "HostPrefill.run -> sgqa_prefill per 4,096-row chunk, copies overlapped on two more streams"}
+               "api": "sgqa_prefill_host (C ABI): pinned host buffers in and out, 4,096-row chunks pipelined by the "
+                      "library over its copy-in stream, the calling stream and its copy-out stream"}
         del hp, host
 
     # ---- CPU baseline (oracle), rank 0 only ----
@@ -394,7 +463,8 @@ def run_sgqa(args, rank, world, local_rank):
                 break
             n2 = int(min(wl.T, max(nrows + 1, nrows * 15.0 / max(secs, 1e-3))))
             rate, secs, nrows, cores = cpu_oracle_rate(hv, wl, n_rows=n2, seed=1 + attempt)
-        cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+        cpu = {"value": round(rate, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
+               "nproc": os.cpu_count(),
                "sample": f"{nrows} query tokens drawn uniformly from the {wl.name} workload, all {wl.G} groups "
                          f"(indexer + top-k + attention, fp64) plus the block-index pass prorated; {secs:.1f} s"}
 
@@ -402,6 +472,13 @@ def run_sgqa(args, rank, world, local_rank):
     coverage = None
     if rank == 0 and not args.no_coverage and wl.q_start == 0 and wl.B == 8:
         coverage = coverage_diagnostic(sgqa, gen, wl, inp, plan, dev)
+
+    # ---- decode step (rank 0, one GPU): the decode workload's latency and roofline ----
+    decode = None
+    if rank == 0 and world == 1 and not args.no_decode:
+        del plan
+        torch.cuda.empty_cache()
+        decode = decode_section(args.steps, args.warmup, dev)
 
     # K1 once, K2 + top-k per 8,192-row pass (top-k in two launches for rows past 16,384
     # candidates: per-slice selection, then the merge), K4 once
@@ -432,11 +509,14 @@ def run_sgqa(args, rank, world, local_rank):
         },
         "stages": stages,
         "layer_roofline_ms": round(layer_roof, 4),
+        "layer_roofline_note": "sum of the stage rooflines (K1 bytes; K2+K3 materialised scores; K4 max of useful "
+                               "FLOPs at the bf16 peak and compulsory bytes at HBM) over the step time",
         "layer_roofline_frac": round(layer_roof / ms, 4),
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "coverage": coverage,
+        "decode": decode,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
         "peaks": {"hbm_gbs": hbm, "bf16_tflops": bf16, "bf16_tflops_sustained": bf16_sus, "source": peak_src},
@@ -448,18 +528,9 @@ def run_sgqa(args, rank, world, local_rank):
 # decode step timing (not the headline metric; reported for the decode workload)
 # ---------------------------------------------------------------------------------------
 
-def run_decode(args, local_rank, fp8=False):
-    """Decode step latency; with fp8 the block-proxy cache is FP8 E4M3 (sgqa_decode_fp8)."""
-    from block_sparse_long_18_b300 import build as _build
-
-    _build.build()
-    from block_sparse_long_18_b300 import inputs as gen
-    from block_sparse_long_18_b300 import sgqa
-
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    wl = gen.WORKLOADS["decode"]
-    inp = gen.make_decode_inputs(wl, seed=0, device=dev)
+def decode_measure(sgqa, wl, inp, dev, steps, warmup, fp8=False):
+    """Decode step latency over one set of decode inputs; with fp8 the block-proxy cache is
+    FP8 E4M3 (sgqa_decode_fp8).  L2 is flushed before every step."""
     prm = sgqa.params(G=wl.G, Hg=wl.Hg, D=wl.D, P=wl.P, B=wl.B, k=wl.k)
     total = inp.k.shape[1]
     batch = len(inp.ctx_len)
@@ -480,12 +551,12 @@ def run_decode(args, local_rank, fp8=False):
         decode(prm, inp.ctx_len, inp.kv_off, inp.q, inp.q_proxy, inp.gate, inp.k, inp.v, inp.k_proxy,
                k_blk, sel, cnt, out, lse, ws)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         flush.fill_(1)
         step()
     torch.cuda.synchronize(dev)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for s in range(args.steps):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s in range(steps):
         flush.fill_(s & 0xFF)
         ev[s][0].record()
         step()
@@ -498,19 +569,55 @@ def run_decode(args, local_rank, fp8=False):
     idx_bytes = wl.G * nb * wl.P * (1 if fp8 else 2)
     gather = wl.G * sum(min(wl.k, (L - 1) // wl.B + 1) for L in inp.ctx_len) * wl.B * wl.D * 2 * 2
     hbm, _, _, src = load_peaks()
+    roof_bytes = idx_bytes + gather + 8 * wl.G * nb        # + scores written and read once
+    roof_ms = roof_bytes / (hbm * 1e9) * 1e3
+    del k_blk, ws, flush
+    return {"ms_per_step": round(ms, 4), "tokens_per_s": round(batch / (ms / 1e3), 1),
+            "roofline": {"bound": "hbm", "algorithmic_bytes": roof_bytes, "roofline_ms": round(roof_ms, 4),
+                         "frac": round(roof_ms / ms, 4), "peak": hbm, "peak_source": src}}
+
+
+def run_decode(args, local_rank, fp8=False):
+    """The decode workload on its own: one JSON line of decode step latency."""
+    from block_sparse_long_18_b300 import build as _build
+
+    _build.build()
+    from block_sparse_long_18_b300 import inputs as gen
+    from block_sparse_long_18_b300 import sgqa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = gen.WORKLOADS["decode"]
+    inp = gen.make_decode_inputs(wl, seed=0, device=dev)
+    r = decode_measure(sgqa, wl, inp, dev, args.steps, args.warmup, fp8=fp8)
+    batch = len(inp.ctx_len)
     return {
         "metric": "Sparse GQA decode step latency (8 sequences, 256K-1M context)",
-        "value": round(ms, 4), "unit": "ms/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
-        "warmup": args.warmup, "tokens_per_s": round(batch / (ms / 1e3), 1),
+        "value": r["ms_per_step"], "unit": "ms/step", "higher_is_better": False, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "tokens_per_s": r["tokens_per_s"],
         "dtype": "bf16 (block-proxy cache e4m3)" if fp8 else "bf16", "data": "synthetic",
         "config": {"workload": f"decode{'_fp8' if fp8 else ''}: {batch} sequences, ctx_len {inp.ctx_len}, "
                                f"G={wl.G} x Hg={wl.Hg}, D={wl.D}, P={wl.P}, block {wl.B}, top-k {wl.k}"
                                + (", block-proxy cache FP8 E4M3" if fp8 else ""),
                    "l2": "flushed before every step"},
-        "roofline": {"bound": "hbm", "algorithmic_bytes": idx_bytes + gather + 4 * wl.G * nb * 2,
-                     "roofline_ms": round((idx_bytes + gather + 8 * wl.G * nb) / (hbm * 1e9) * 1e3, 4),
-                     "peak": hbm, "peak_source": src},
+        "roofline": r["roofline"],
     }
+
+
+def decode_section(steps, warmup, dev):
+    """The decode workload (8 sequences, 256K-1M context) measured inside the default run:
+    bf16 and FP8 E4M3 block-proxy caches over the same inputs."""
+    from block_sparse_long_18_b300 import inputs as gen
+    from block_sparse_long_18_b300 import sgqa
+
+    wl = gen.WORKLOADS["decode"]
+    inp = gen.make_decode_inputs(wl, seed=0, device=dev)
+    out = {"workload": f"decode: {len(inp.ctx_len)} sequences, ctx_len {inp.ctx_len}, top-k {wl.k} blocks of {wl.B}",
+           "bf16_cache": decode_measure(sgqa, wl, inp, dev, max(steps, 10), warmup),
+           "fp8_e4m3_cache": decode_measure(sgqa, wl, inp, dev, max(steps, 10), warmup, fp8=True)}
+    del inp
+    torch.cuda.empty_cache()
+    return out
 
 
 # ---------------------------------------------------------------------------------------
@@ -554,6 +661,7 @@ def run_reference(args, rank, world):
         "config": {"workload": f"{wl.name}: prefill T={wl.T}, context {wl.C}, G={wl.G} x Hg={wl.Hg}, D={wl.D}, "
                                f"P={wl.P}, block {wl.B}, top-k {wl.k}", "global_batch": 1, "seq_len": wl.T},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle", "cores": oracle.num_threads(),
+                         "cpu_model": cpu_model(), "nproc": os.cpu_count(),
                          "sample": f"{n_rows} query tokens per step drawn uniformly from the {wl.name} workload, all "
                                    f"{wl.G} groups (indexer + top-k + attention, fp64), block-index pass prorated"},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -570,6 +678,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-coverage", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -40,12 +40,19 @@ constexpr int K4U_CB = 16;                          // union blocks per chunk (1
 constexpr uint32_t K4U_SLOT = K4U_CB * 3072;        // one chunk of K (or V): 48 KB
 constexpr int K4U_MAXU = 4096;                      // union capacity: 8 rows x 512 blocks
 constexpr int K4U_WIN = 16384;                      // blocks covered by one builder bitmap
-constexpr int K4U_MAX_BLOCKS = 65536;               // union entries are 16-bit block indices
-// one table buffer: union blocks (u16), per-row membership bits over union positions, meta
+constexpr int K4U_MAX_WIN = 16;                     // windows a unit's blocks may span
+constexpr int K4U_MAX_BLOCKS = K4U_WIN * K4U_MAX_WIN;  // 262,144 blocks: positions below 2,097,152
+// one table buffer: union entries (u16: block offset inside its window), per-row membership
+// bits over union positions, meta
 constexpr uint32_t K4U_TB_UBLK = 0;
 constexpr uint32_t K4U_TB_RBITS = 2 * K4U_MAXU;              // uint32 [8][K4U_MAXU / 32]
-constexpr uint32_t K4U_TB_META = K4U_TB_RBITS + 8 * (K4U_MAXU / 8);  // int32: nU, own position [8]
+constexpr uint32_t K4U_TB_META = K4U_TB_RBITS + 8 * (K4U_MAXU / 8);
+// meta, int32: [0] nU, [1..8] own position per row, [9] windows used, [10..25] the union
+// position at which each window's entries start (ascending; an empty window repeats the
+// next start)
+constexpr int K4U_META_NWIN = 9, K4U_META_WSTART = 10;
 constexpr uint32_t K4U_TB = K4U_TB_META + 128;
+static_assert((K4U_META_WSTART + K4U_MAX_WIN) * 4 <= 128, "k4u table meta");
 constexpr uint32_t K4U_K_OFF = 0;
 constexpr uint32_t K4U_V_OFF = 2 * K4U_SLOT;
 constexpr uint32_t K4U_T_OFF = 4 * K4U_SLOT;
@@ -164,8 +171,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       int32_t bmax = bt_l;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) bmax = max(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
-      int32_t nU = 0;
-      for (int32_t wb = 0; wb <= bmax; wb += K4U_WIN) {
+      int32_t nU = 0, nwin = 0;
+      for (int32_t wb = 0; wb <= bmax; wb += K4U_WIN, ++nwin) {
+        if (lane == 0) meta[K4U_META_WSTART + nwin] = nU;
         for (int w = lane; w < K4U_WIN / 32; w += 32) bm[w] = 0u;
         __syncwarp();
         for (int r0 = 0; r0 < 8; r0 += 2) {  // two rows' entries in flight at once
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
           while (bits) {
             const uint32_t bit = __ffs(bits) - 1;
             bits &= bits - 1;
-            ublk[run++] = (uint16_t)(wb + 32 * wi + bit);
+            ublk[run++] = (uint16_t)(32 * wi + bit);
           }
         }
         nU += (int32_t)__shfl_sync(0xffffffffu, incl, 31);
@@ -256,10 +264,17 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         __syncwarp();
       }
       if (nU == 0) {  // only after bad input: one fully masked block keeps every role in step
-        if (lane == 0) ublk[0] = 0;
+        if (lane == 0) {
+          ublk[0] = 0;
+          meta[K4U_META_WSTART] = 0;
+        }
         nU = 1;
+        nwin = 1;
       }
-      if (lane == 0) meta[0] = nU;
+      if (lane == 0) {
+        meta[0] = nU;
+        meta[K4U_META_NWIN] = nwin;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kTblFull + buf));
     }
@@ -280,7 +295,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       const int32_t g = (int32_t)(u / ntiles);
       const uint8_t* T = tbl(buf);
       const uint16_t* ublk = reinterpret_cast<const uint16_t*>(T + K4U_TB_UBLK);
-      const int32_t nU = reinterpret_cast<const int32_t*>(T + K4U_TB_META)[0];
+      const int32_t* meta = reinterpret_cast<const int32_t*>(T + K4U_TB_META);
+      const int32_t nU = meta[0], nwin = meta[K4U_META_NWIN];
       const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
       const int64_t row0 = (int64_t)g * a.ctx_cap;
       for (int32_t c = 0; c < nch; ++c) {
@@ -293,8 +309,13 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         ok = __shfl_sync(0xffffffffu, r, 0) != 0;
         if (!ok) break;
         if (lane < K4U_CB) {
-          const int32_t p = c * K4U_CB + (int32_t)lane;
-          const int32_t b = ublk[p < nU ? p : nU - 1];  // past the union: a valid block, masked
+          int32_t p = c * K4U_CB + (int32_t)lane;
+          p = p < nU ? p : nU - 1;  // past the union: a valid block, masked
+          // the window holding position p: the last one whose entries start at or before p
+          int32_t w = 0;
+#pragma unroll
+          for (int x = 1; x < K4U_MAX_WIN; ++x) w += (x < nwin && meta[K4U_META_WSTART + x] <= p) ? 1 : 0;
+          const int32_t b = w * K4U_WIN + (int32_t)ublk[p];
           tma_load_3d_hint(base0 + slot * K4U_SLOT + lane * 3072, map, bar(full0 + slot), 0,
                            (int32_t)(row0 + (int64_t)b * 8), 0, keep);
         }

@@ -21,7 +21,6 @@
 #include "k2d_decode_index.cuh"
 #include "k3_topk.cuh"
 #include "k4_attention.cuh"
-#include "k4tc_attention.cuh"
 #include "k4u_attention.cuh"
 
 using namespace sgqa;
@@ -46,7 +45,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Parameters after defaults are resolved.
 struct Prm {
-  int G, Hg, H, D, P, B, k, gate_per_dim;
+  int G, Hg, H, D, P, B, k, gate_per_dim, attn_kernel;
   float scale;
 };
 
@@ -60,6 +59,8 @@ sgqa_status check_params(const sgqa_params* p, Prm& o) {
   const int B = p->block_size;
   if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED_SHAPE;
   if (p->gate_per_dim != 0 && p->gate_per_dim != 1) return SGQA_ERR_INVALID_ARGUMENT;
+  if (p->attn_kernel != SGQA_ATTN_AUTO && p->attn_kernel != SGQA_ATTN_WARP && p->attn_kernel != SGQA_ATTN_TC_UNION)
+    return SGQA_ERR_INVALID_ARGUMENT;
   o.G = p->num_kv_groups;
   o.Hg = p->heads_per_group;
   o.H = o.G * o.Hg;
@@ -68,6 +69,7 @@ sgqa_status check_params(const sgqa_params* p, Prm& o) {
   o.B = B;
   o.k = p->top_k_blocks;
   o.gate_per_dim = p->gate_per_dim;
+  o.attn_kernel = p->attn_kernel;
   o.scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / std::sqrt((float)o.D);
   return SGQA_OK;
 }
@@ -102,15 +104,45 @@ bool make_map_3d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint6
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- per-device launch state ----
+// The SM count and the kernels whose dynamic shared-memory limit has been raised, kept per
+// device under one mutex: a process may drive several devices, from several threads.
+constexpr int kMaxDevices = 64;
+struct DevState {
+  int sms = 0;
+  uint32_t attr_done = 0;  // bit per AttrKernel
+};
+std::mutex g_dev_mu;
+DevState g_dev[kMaxDevices];
+
+int current_device() {
+  int d = -1;
+  return cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices ? d : -1;
+}
+
 int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
+  const int dev = current_device();
+  if (dev < 0) return 148;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (g_dev[dev].sms == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    g_dev[dev].sms = n;
   }
-  return n;
+  return g_dev[dev].sms;
+}
+
+enum AttrKernel { kAttrK2 = 0, kAttrK4Tma = 1, kAttrK4Cp = 2, kAttrK4U = 3 };
+
+// Raises the dynamic shared-memory limit of `fn` to `bytes` once per device.
+cudaError_t ensure_smem_attr(AttrKernel which, const void* fn, size_t bytes) {
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (g_dev[dev].attr_done & (1u << which)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) g_dev[dev].attr_done |= 1u << which;
+  return e;
 }
 
 // ---- attention launch: 8 warps (units) per CTA, two stages each ----
@@ -121,13 +153,9 @@ template <bool TMA>
 cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
                         cudaStream_t st) {
   const size_t smem = k4_smem(kK4Warps);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k4_sparse_attn<kK4Warps, TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t e = ensure_smem_attr(TMA ? kAttrK4Tma : kAttrK4Cp,
+                                         reinterpret_cast<const void*>(k4_sparse_attn<kK4Warps, TMA>), smem);
+  if (e != cudaSuccess) return e;
   const int64_t grid = cdiv(n_units, kK4Warps);
   k4_sparse_attn<kK4Warps, TMA><<<(unsigned)grid, kK4Warps * 32, smem, st>>>(a, tk, tv);
   return cudaGetLastError();
@@ -146,13 +174,8 @@ bool make_kv_map(CUtensorMap* m, const void* base, uint64_t tokens) {
 
 cudaError_t launch_k2(const K2Args& a, const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc,
                       cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k2_indexer, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K2_SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t e = ensure_smem_attr(kAttrK2, reinterpret_cast<const void*>(k2_indexer), K2_SMEM_BYTES);
+  if (e != cudaSuccess) return e;
   const int64_t grid = std::min<int64_t>(a.n_items, num_sms());
   if (grid <= 0) return cudaSuccess;
   k2_indexer<<<(unsigned)grid, K2_THREADS, K2_SMEM_BYTES, st>>>(a, ta, tb, tc);
@@ -304,61 +327,29 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
   return SGQA_OK;
 }
 
-// Which attention kernel serves prefill: the tcgen05 one for blocks of 8 or 16 tokens
-// (the TMA gathers land in whole 1 KB swizzle atoms), the warp-level one otherwise.
-bool use_k4tc(const Prm& p) {
-  static const int forced = [] {
-    const char* e = std::getenv("SGQA_K4_IMPL");
-    return e ? (std::strcmp(e, "mma") == 0 ? 0 : (std::strcmp(e, "tc") == 0 ? 1 : -1)) : -1;
-  }();
-  return forced == 1 && p.B == 8;
+// The union kernel serves a prefill call when its shape holds: blocks of 8, 16 heads per
+// group, at most 512 selected blocks per row (a unit's union fits its 4,096-entry table),
+// block indices below K4U_MAX_BLOCKS, not dense mode.
+bool union_fits(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
+  return p.B == 8 && p.Hg == 16 && p.k <= 512 && !dense && T > 0 &&
+         (q_start + T - 1) / 8 < (int64_t)K4U_MAX_BLOCKS;
 }
 
-cudaError_t launch_k4tc(const K4TArgs& a, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                        cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k4tc_sparse_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K4T_SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
+// The attention kernel a call launches (SGQA_ATTN_WARP or SGQA_ATTN_TC_UNION), following
+// sgqa_params.attn_kernel; -1 when the requested kernel cannot serve these arguments.
+int attn_choice(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
+  const bool fits = union_fits(p, dense, T, q_start);
+  switch (p.attn_kernel) {
+    case SGQA_ATTN_AUTO: return fits ? SGQA_ATTN_TC_UNION : SGQA_ATTN_WARP;
+    case SGQA_ATTN_WARP: return SGQA_ATTN_WARP;
+    case SGQA_ATTN_TC_UNION: return fits ? SGQA_ATTN_TC_UNION : -1;
   }
-  const int64_t grid = std::min<int64_t>(a.rows, num_sms());
-  if (grid <= 0) return cudaSuccess;
-  for (int g = 0; g < a.G; ++g) {  // one launch per KV group
-    K4TArgs ag = a;
-    ag.g_first = g;
-    ag.g_count = 1;
-    k4tc_sparse_attn<<<(unsigned)grid, K4T_THREADS, K4T_SMEM, st>>>(ag, tq, tk, tv);
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  return cudaSuccess;
-}
-
-// The union kernel serves prefill by default when its shape holds: blocks of 8, 16 heads
-// per group, at most 512 selected blocks per row (a unit's union fits its 4,096-entry
-// table), block indices below 65,536 (16-bit table entries), not dense mode.  Otherwise
-// the warp-level kernel runs.  SGQA_K4_IMPL=mma|tc|union overrides.
-bool use_k4u(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
-  static const int forced = [] {
-    const char* e = std::getenv("SGQA_K4_IMPL");
-    if (!e) return -1;
-    if (std::strcmp(e, "union") == 0) return 1;
-    if (std::strcmp(e, "mma") == 0 || std::strcmp(e, "tc") == 0) return 0;
-    return -1;
-  }();
-  const bool fits = p.B == 8 && p.Hg == 16 && p.k <= 512 && !dense && T > 0 &&
-                    (q_start + T - 1) / 8 < (int64_t)K4U_MAX_BLOCKS;
-  return fits && forced != 0;
+  return -1;
 }
 
 cudaError_t launch_k4u(const K4UArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k4u_sparse_attn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)K4U_SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  const cudaError_t e = ensure_smem_attr(kAttrK4U, reinterpret_cast<const void*>(k4u_sparse_attn), K4U_SMEM);
+  if (e != cudaSuccess) return e;
   const int64_t n_units = (int64_t)a.G * cdiv(a.rows, 8);
   const int64_t grid = std::min<int64_t>(n_units, num_sms());
   if (grid <= 0) return cudaSuccess;
@@ -369,7 +360,9 @@ cudaError_t launch_k4u(const K4UArgs& a, const CUtensorMap& tk, const CUtensorMa
 sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void* v, int64_t ctx_cap, const void* gate,
                           const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T, int64_t q_start, void* out,
                           float* lse, int32_t dense, cudaStream_t st) {
-  if (use_k4u(p, dense, T, q_start)) {
+  const int kernel = attn_choice(p, dense, T, q_start);
+  if (kernel < 0) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (kernel == SGQA_ATTN_TC_UNION) {
     K4UArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.gate = static_cast<const __nv_bfloat16*>(gate);
@@ -390,34 +383,6 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
     const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
     if (!make_kv_map(&tk, k, rowsz) || !make_kv_map(&tv, v, rowsz)) return SGQA_ERR_CUDA;
     SGQA_CUDA_OK(launch_k4u(a, tk, tv, st));
-    return SGQA_OK;
-  }
-  if (use_k4tc(p)) {
-    K4TArgs a{};
-    a.gate = static_cast<const __nv_bfloat16*>(gate);
-    a.out = static_cast<__nv_bfloat16*>(out);
-    a.lse = lse;
-    a.sel_idx = sel_idx;
-    a.sel_cnt = sel_cnt;
-    a.rows = T;
-    a.pos0 = q_start;
-    a.ctx_cap = ctx_cap;
-    a.G = p.G;
-    a.Hg = p.Hg;
-    a.H = p.H;
-    a.B = p.B;
-    a.kcap = p.k;
-    a.scale_log2 = p.scale * 1.4426950408889634f;
-    a.dense = dense;
-    a.gate_per_dim = p.gate_per_dim;
-    a.wait_ns = g_wait_ns;
-    CUtensorMap tq, tk, tv;
-    const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
-    if (!make_map_3d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, 64, 3, (uint64_t)T * p.H, 128, 384, 64, 1, 16))
-      return SGQA_ERR_CUDA;
-    if (!make_kv_map(&tk, k, rowsz) || !make_kv_map(&tv, v, rowsz)) return SGQA_ERR_CUDA;
-    a.block_major = 1;
-    SGQA_CUDA_OK(launch_k4tc(a, tq, tk, tv, st));
     return SGQA_OK;
   }
   K4Args a{};
@@ -458,7 +423,6 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
 // code must not pass the symbol itself to a kernel (in host code it names a host-side
 // stand-in); its device address is looked up once per device with cudaGetSymbolAddress.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[SGQA_NOALLOC_SCRATCH_BYTES];
-constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[kMaxDevices] = {};
 
@@ -473,6 +437,80 @@ sgqa_status noalloc_scratch_address(void** out) {
   }
   *out = g_noalloc_addr[dev];
   return SGQA_OK;
+}
+
+
+// ---- end-to-end prefill from host memory: chunk layout and per-device copy streams ----
+constexpr int64_t kHostChunkRows = 4096;  // default query rows per pipelined chunk
+constexpr int kHostRing = 4;              // events per kind; chunk j uses slot j % kHostRing
+
+// Rows per chunk: chunk_rows (default kHostChunkRows) rounded down to a multiple of B,
+// at least B, at most T rounded up to B.
+int64_t host_chunk_rows(const Prm& p, int64_t T, int64_t chunk_rows) {
+  int64_t R = chunk_rows > 0 ? chunk_rows : kHostChunkRows;
+  R = std::min<int64_t>(R, cdiv(std::max<int64_t>(T, 1), p.B) * p.B);
+  return std::max<int64_t>(p.B, R / p.B * p.B);
+}
+
+// Workspace of sgqa_prefill_host: two q_proxy chunk buffers [G, R, P] (chunk j + 1 is
+// copied in while chunk j is computed), the chunk's selection [G, R, k] and counts [G, R],
+// then the indexer + top-k workspace of one chunk.
+struct HostWs {
+  size_t qp[2], sel, cnt, index, index_bytes, total;
+};
+HostWs host_ws_layout(const Prm& p, int64_t R, int64_t ctx_len) {
+  HostWs w{};
+  const size_t qp = align_up((size_t)p.G * R * p.P * 2, 256);
+  w.qp[0] = 0;
+  w.qp[1] = qp;
+  w.sel = 2 * qp;
+  w.cnt = w.sel + align_up((size_t)p.G * R * p.k * 4, 256);
+  w.index = w.cnt + align_up((size_t)p.G * R * 4, 256);
+  w.index_bytes = std::max<size_t>(256, index_ws_bytes(p, R, (ctx_len - 1) / p.B));
+  w.total = w.index + w.index_bytes;
+  return w;
+}
+
+// Two non-blocking copy streams (host to device, device to host) and the pipeline's events,
+// created on a device's first sgqa_prefill_host call and kept until the process exits.
+// The mutex is held while a call enqueues its work, so calls from several host threads
+// do not interleave their use of the shared events.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  cudaEvent_t begin = nullptr, end = nullptr, copied[kHostRing] = {}, done[kHostRing] = {};
+  std::mutex mu;
+};
+HostPipe g_pipe[kMaxDevices];
+
+sgqa_status host_pipe(HostPipe** out) {
+  const int dev = current_device();
+  if (dev < 0) return SGQA_ERR_CUDA;
+  HostPipe& h = g_pipe[dev];
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!h.ready) {
+      const unsigned ef = cudaEventDisableTiming;
+      bool ok = cudaStreamCreateWithFlags(&h.s_in, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaStreamCreateWithFlags(&h.s_out, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h.begin, ef) == cudaSuccess &&
+                cudaEventCreateWithFlags(&h.end, ef) == cudaSuccess;
+      for (int i = 0; ok && i < kHostRing; ++i)
+        ok = cudaEventCreateWithFlags(&h.copied[i], ef) == cudaSuccess &&
+             cudaEventCreateWithFlags(&h.done[i], ef) == cudaSuccess;
+      if (!ok) return SGQA_ERR_CUDA;  // partial objects stay allocated; the next call retries the rest
+      h.ready = true;
+    }
+  }
+  *out = &h;
+  return SGQA_OK;
+}
+
+// Copies G rows of `bytes` each, `pitch_src` / `pitch_dst` apart (one strided copy).
+cudaError_t copy_rows(void* dst, size_t pitch_dst, const void* src, size_t pitch_src, size_t bytes, size_t rows,
+                      cudaMemcpyKind kind, cudaStream_t st) {
+  if (bytes == 0 || rows == 0) return cudaSuccess;
+  return cudaMemcpy2DAsync(dst, pitch_dst, src, pitch_src, bytes, rows, kind, st);
 }
 
 }  // namespace
@@ -497,9 +535,7 @@ int32_t sgqa_abi_version(void) { return SGQA_ABI_VERSION; }
 int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode) {
   Prm p;
   if (check_params(prm, p) != SGQA_OK || T < 0 || q_start < 0) return -1;
-  if (use_k4u(p, dense_mode, T, q_start)) return SGQA_ATTN_TC_UNION;
-  if (use_k4tc(p)) return SGQA_ATTN_TC_ROW;
-  return SGQA_ATTN_WARP;
+  return attn_choice(p, dense_mode ? 1 : 0, T, q_start);
 }
 
 sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns) {
@@ -532,6 +568,8 @@ size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64
       return std::max<size_t>(256, index_ws_bytes(p, std::min<int64_t>(std::max<int64_t>(T, 1), kIndexChunkRows), max_cand));
     case SGQA_OP_ATTN:
       return 256;
+    case SGQA_OP_PREFILL_HOST:
+      return host_ws_layout(p, host_chunk_rows(p, T, batch), ctx_len).total;
     case SGQA_OP_DECODE: {
       if (batch < 1 || batch > kMaxBatch) return 0;
       const size_t sc = index_ws_bytes(p, batch, max_cand);
@@ -654,6 +692,95 @@ sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, c
   s = sgqa_index_topk(prm, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, ws_bytes, stream);
   if (s != SGQA_OK) return s;
   return sgqa_sparse_attn_fwd(prm, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, 0, stream);
+}
+
+sgqa_status sgqa_prefill_host(const sgqa_params* prm, const sgqa_host_tensors* host, const sgqa_device_tensors* dev,
+                              int64_t ctx_cap, int64_t T, int64_t q_start, int64_t chunk_rows, sgqa_stream_t stream) {
+  Prm p;
+  sgqa_status s = check_params(prm, p);
+  if (s != SGQA_OK) return s;
+  if (!host || !dev) return SGQA_ERR_INVALID_ARGUMENT;
+  const sgqa_host_tensors& h = *host;
+  const sgqa_device_tensors& d = *dev;
+  if (!h.q || !h.k || !h.v || !h.gate || !h.q_proxy || !h.k_proxy || !h.out) return SGQA_ERR_INVALID_ARGUMENT;
+  if (!d.q || !d.k || !d.v || !d.gate || !d.k_proxy || !d.k_blk || !d.out) return SGQA_ERR_INVALID_ARGUMENT;
+  if (h.lse && !d.lse) return SGQA_ERR_INVALID_ARGUMENT;
+  if (T < 0 || q_start < 0 || q_start + T > ctx_cap) return SGQA_ERR_INVALID_ARGUMENT;
+  if (T == 0) return SGQA_OK;
+  if (cdiv(q_start + T, p.B) > d.nb_cap) return SGQA_ERR_INVALID_ARGUMENT;
+  if ((int64_t)p.G * ctx_cap > (int64_t)INT32_MAX) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  const int64_t R = host_chunk_rows(p, T, chunk_rows);
+  const HostWs wl = host_ws_layout(p, R, q_start + T);
+  if (!d.ws || d.ws_bytes < wl.total) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(d.ws)) return SGQA_ERR_INVALID_ARGUMENT;
+  // the same checks sgqa_prefill makes on every chunk, made once before anything is enqueued
+  if (attn_choice(p, 0, std::min(T, R), q_start) < 0 || attn_choice(p, 0, T - (T - 1) / R * R, q_start + (T - 1) / R * R) < 0)
+    return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(d.q) || !aligned16(d.k) || !aligned16(d.v) || !aligned16(d.out) || !aligned16(d.k_proxy) ||
+      !aligned16(d.k_blk) || (p.gate_per_dim && !aligned16(d.gate)))
+    return SGQA_ERR_INVALID_ARGUMENT;
+  HostPipe* pp = nullptr;
+  s = host_pipe(&pp);
+  if (s != SGQA_OK) return s;
+  std::lock_guard<std::mutex> lock(pp->mu);
+  cudaStream_t comp = reinterpret_cast<cudaStream_t>(stream);
+  const size_t D2 = (size_t)p.D * 2, P2 = (size_t)p.P * 2;
+  const size_t row_q = (size_t)p.H * D2;                        // bytes of one query row of q / out
+  const size_t row_g = p.gate_per_dim ? row_q : (size_t)p.H * 2;  // of gate
+  uint8_t* ws = static_cast<uint8_t*>(d.ws);
+  auto dq = static_cast<uint8_t*>(d.q);
+  auto dg = static_cast<uint8_t*>(d.gate);
+  auto dout = static_cast<uint8_t*>(d.out);
+  auto hq = static_cast<const uint8_t*>(h.q);
+  auto hg = static_cast<const uint8_t*>(h.gate);
+  auto hqp = static_cast<const uint8_t*>(h.q_proxy);
+  auto hout = static_cast<uint8_t*>(h.out);
+
+  SGQA_CUDA_OK(cudaEventRecord(pp->begin, comp));
+  SGQA_CUDA_OK(cudaStreamWaitEvent(pp->s_in, pp->begin, 0));
+  SGQA_CUDA_OK(cudaStreamWaitEvent(pp->s_out, pp->begin, 0));
+  int64_t ctx_done = 0;  // cache positions copied so far
+  for (int64_t j = 0, a = 0; a < T; ++j, a += R) {
+    const int64_t rows = std::min(R, T - a);
+    const int slot = (int)(j % kHostRing);
+    void* qp = ws + wl.qp[j & 1];
+    // ---- copy-in (s_in): the cache up to the chunk's last position, then its query rows ----
+    if (j >= 2) SGQA_CUDA_OK(cudaStreamWaitEvent(pp->s_in, pp->done[(j - 2) % kHostRing], 0));  // qp[j & 1] is free
+    const int64_t hi = q_start + a + rows;
+    const size_t c0 = (size_t)ctx_done, cl = (size_t)(hi - ctx_done);
+    SGQA_CUDA_OK(copy_rows(static_cast<uint8_t*>(d.k) + c0 * D2, ctx_cap * D2, static_cast<const uint8_t*>(h.k) + c0 * D2,
+                           ctx_cap * D2, cl * D2, p.G, cudaMemcpyHostToDevice, pp->s_in));
+    SGQA_CUDA_OK(copy_rows(static_cast<uint8_t*>(d.v) + c0 * D2, ctx_cap * D2, static_cast<const uint8_t*>(h.v) + c0 * D2,
+                           ctx_cap * D2, cl * D2, p.G, cudaMemcpyHostToDevice, pp->s_in));
+    SGQA_CUDA_OK(copy_rows(static_cast<uint8_t*>(d.k_proxy) + c0 * P2, ctx_cap * P2,
+                           static_cast<const uint8_t*>(h.k_proxy) + c0 * P2, ctx_cap * P2, cl * P2, p.G,
+                           cudaMemcpyHostToDevice, pp->s_in));
+    SGQA_CUDA_OK(cudaMemcpyAsync(dq + a * row_q, hq + a * row_q, rows * row_q, cudaMemcpyHostToDevice, pp->s_in));
+    SGQA_CUDA_OK(cudaMemcpyAsync(dg + a * row_g, hg + a * row_g, rows * row_g, cudaMemcpyHostToDevice, pp->s_in));
+    SGQA_CUDA_OK(copy_rows(qp, rows * P2, hqp + a * P2, T * P2, rows * P2, p.G, cudaMemcpyHostToDevice, pp->s_in));
+    SGQA_CUDA_OK(cudaEventRecord(pp->copied[slot], pp->s_in));
+    ctx_done = hi;
+    // ---- compute (stream) ----
+    SGQA_CUDA_OK(cudaStreamWaitEvent(comp, pp->copied[slot], 0));
+    if (j == 0 && q_start > 0) {  // blocks of the cached prefix
+      s = sgqa_build_block_index(prm, d.k_proxy, ctx_cap, 0, q_start, d.k_blk, d.nb_cap, stream);
+      if (s != SGQA_OK) return s;
+    }
+    s = sgqa_prefill(prm, dq + a * row_q, d.k, d.v, dg + a * row_g, qp, d.k_proxy, ctx_cap, rows, q_start + a, d.k_blk,
+                     d.nb_cap, reinterpret_cast<int32_t*>(ws + wl.sel), reinterpret_cast<int32_t*>(ws + wl.cnt),
+                     dout + a * row_q, d.lse ? d.lse + a * p.H : nullptr, ws + wl.index, wl.index_bytes, stream);
+    if (s != SGQA_OK) return s;
+    SGQA_CUDA_OK(cudaEventRecord(pp->done[slot], comp));
+    // ---- copy-out (s_out) ----
+    SGQA_CUDA_OK(cudaStreamWaitEvent(pp->s_out, pp->done[slot], 0));
+    SGQA_CUDA_OK(cudaMemcpyAsync(hout + a * row_q, dout + a * row_q, rows * row_q, cudaMemcpyDeviceToHost, pp->s_out));
+    if (h.lse)
+      SGQA_CUDA_OK(cudaMemcpyAsync(h.lse + a * p.H, d.lse + a * p.H, rows * p.H * sizeof(float), cudaMemcpyDeviceToHost,
+                                   pp->s_out));
+  }
+  SGQA_CUDA_OK(cudaEventRecord(pp->end, pp->s_out));
+  SGQA_CUDA_OK(cudaStreamWaitEvent(comp, pp->end, 0));
+  return SGQA_OK;
 }
 
 static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64_t* ctx_len, const int64_t* kv_off,

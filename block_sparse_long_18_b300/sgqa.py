@@ -37,16 +37,16 @@ STATUS = {
     5: "SGQA_ERR_DEVICE_TIMEOUT",
     6: "SGQA_ERR_DEVICE_BOUNDS",
 }
-SGQA_OP_INDEX_TOPK, SGQA_OP_PREFILL, SGQA_OP_DECODE, SGQA_OP_ATTN = 1, 2, 3, 4
+SGQA_OP_INDEX_TOPK, SGQA_OP_PREFILL, SGQA_OP_DECODE, SGQA_OP_ATTN, SGQA_OP_PREFILL_HOST = 1, 2, 3, 4, 5
 
 # Every symbol include/sgqa.h declares.
 EXPORTS = (
     "sgqa_build_block_index", "sgqa_index_topk", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
     "sgqa_workspace_bytes", "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout",
     "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc", "sgqa_attention_kernel",
-    "sgqa_build_block_index_fp8", "sgqa_decode_fp8",
+    "sgqa_build_block_index_fp8", "sgqa_decode_fp8", "sgqa_prefill_host",
 )
-ATTN_WARP, ATTN_TC_ROW, ATTN_TC_UNION = 0, 1, 2
+ATTN_AUTO, ATTN_WARP, ATTN_TC_UNION = 0, 1, 2
 
 
 class SgqaError(RuntimeError):
@@ -65,13 +65,28 @@ class Params(ctypes.Structure):
         ("top_k_blocks", ctypes.c_int32),
         ("gate_per_dim", ctypes.c_int32),
         ("softmax_scale", ctypes.c_float),
+        ("attn_kernel", ctypes.c_int32),
     ]
 
 
-def params(G=4, Hg=16, D=192, P=256, B=8, k=512, gate_per_dim=1, scale=0.0) -> Params:
+def params(G=4, Hg=16, D=192, P=256, B=8, k=512, gate_per_dim=1, scale=0.0, attn_kernel=ATTN_AUTO) -> Params:
     """Layer constants; the defaults are the pages' (phantomic12 entry: 64 heads in 4 KV
-    groups, head_dim 192, topk 512, proxy_dim 256; ai4snews item: block size 8)."""
-    return Params(G, Hg, D, P, B, k, gate_per_dim, scale)
+    groups, head_dim 192, topk 512, proxy_dim 256; ai4snews item: block size 8).
+    attn_kernel: ATTN_AUTO, or ATTN_WARP / ATTN_TC_UNION to force a prefill attention kernel."""
+    return Params(G, Hg, D, P, B, k, gate_per_dim, scale, attn_kernel)
+
+
+class HostTensors(ctypes.Structure):
+    """sgqa_host_tensors: host pointers of one end-to-end prefill."""
+    _fields_ = [(n, ctypes.c_void_p) for n in ("q", "k", "v", "gate", "q_proxy", "k_proxy", "out", "lse")]
+
+
+class DeviceTensors(ctypes.Structure):
+    """sgqa_device_tensors: the caller's device buffers of one end-to-end prefill."""
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("gate", ctypes.c_void_p),
+                ("k_proxy", ctypes.c_void_p), ("k_blk", ctypes.c_void_p), ("nb_cap", ctypes.c_int64),
+                ("out", ctypes.c_void_p), ("lse", ctypes.c_void_p), ("ws", ctypes.c_void_p),
+                ("ws_bytes", ctypes.c_size_t)]
 
 
 _P = ctypes.c_void_p
@@ -94,12 +109,15 @@ _lib.sgqa_decode.argtypes = [_PP, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P
 _lib.sgqa_decode_fp8.argtypes = [_PP, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
                              ctypes.c_size_t, _P]
 _lib.sgqa_build_block_index_fp8.argtypes = [_PP, _P, _I64, _I64, _I64, _P, _I64, _P]
+_lib.sgqa_prefill_host.argtypes = [_PP, ctypes.POINTER(HostTensors), ctypes.POINTER(DeviceTensors), _I64, _I64, _I64,
+                                   _I64, _P]
 _lib.sgqa_workspace_bytes.restype = ctypes.c_size_t
 _lib.sgqa_workspace_bytes.argtypes = [_PP, ctypes.c_int32, _I64, _I64, ctypes.c_int32]
 _lib.sgqa_get_device_error.argtypes = [_P]
 _lib.sgqa_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
 _lib.sgqa_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _P]
-for _f in ("sgqa_build_block_index", "sgqa_index_topk", "sgqa_index_topk_noalloc", "sgqa_sparse_attn_fwd", "sgqa_prefill", "sgqa_decode",
+for _f in ("sgqa_build_block_index", "sgqa_index_topk", "sgqa_index_topk_noalloc", "sgqa_sparse_attn_fwd",
+           "sgqa_prefill", "sgqa_prefill_host", "sgqa_decode", "sgqa_decode_fp8", "sgqa_build_block_index_fp8",
            "sgqa_get_device_error", "sgqa_set_wait_timeout_ns", "sgqa_selftest_wait_timeout"):
     getattr(_lib, _f).restype = ctypes.c_int
 
@@ -289,87 +307,73 @@ def prefill(prm: Params, q, k, v, gate, q_proxy, k_proxy, q_start: int = 0, k_bl
     return plan.run(q, k, v, gate, q_proxy, k_proxy)
 
 
+def _host(t: torch.Tensor | None, dtype, name: str, shape=None):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {dtype} host tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t.data_ptr()
+
+
+def sgqa_prefill_host(prm: Params, host: dict, dev: dict, q_start: int = 0, chunk_rows: int = 0, stream=None):
+    """End-to-end prefill from host tensors (sgqa_prefill_host).  host: q, k, v, gate,
+    q_proxy, k_proxy, out and optionally lse (pinned host tensors); dev: the device
+    buffers q, k, v, gate, k_proxy, k_blk, out, lse (or None) and ws."""
+    T = host["q"].shape[0]
+    ctx_cap = host["k"].shape[1]
+    lse_h = host.get("lse")
+    ht = HostTensors(*[_host(host[n], BF16, n) for n in ("q", "k", "v", "gate", "q_proxy", "k_proxy", "out")],
+                     _host(lse_h, F32, "lse"))
+    dv = lambda n, dt=BF16: _dev(dev[n], dt, n)
+    dt = DeviceTensors(dv("q"), dv("k"), dv("v"), dv("gate"), dv("k_proxy"), dv("k_blk"), dev["k_blk"].shape[1],
+                       dv("out"), _dev(dev.get("lse"), F32, "lse"), _dev(dev["ws"], torch.uint8, "ws"),
+                       dev["ws"].numel())
+    _check(_lib.sgqa_prefill_host(ctypes.byref(prm), ctypes.byref(ht), ctypes.byref(dt), ctx_cap, T, q_start,
+                                  chunk_rows, _stream(stream)), "sgqa_prefill_host")
+
+
 class HostPrefill:
-    """End-to-end prefill from HOST (pinned) tensors, pipelined over chunks of query rows.
+    """End-to-end prefill from HOST (pinned) tensors through sgqa_prefill_host: the library
+    pipelines chunks of query rows over its copy-in stream, the calling stream and its
+    copy-out stream.  This class only keeps the device buffers and the pinned output
+    between calls.  The calling stream (or the current one) waits for the last copy back,
+    so events recorded on it around `run` time the whole job."""
 
-    Chunk j (rows [a, b)) needs the K/V/proxy cache up to position q_start + b only
-    (causality), so its copies in, its layer call (a chunked prefill at q_start + a) and
-    its output copy back run on three streams and overlap with the neighbouring chunks:
-    copy-in of chunk j+1 and copy-out of chunk j-1 proceed while chunk j is computed.
-    Device buffers are kept between calls.  The calling stream (or the current one) waits
-    for the last copy back, so events recorded on it around `run` time the whole job."""
-
-    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda", chunk_rows: int = 4096):
-        self.prm, self.T, self.ctx_cap, self.q_start = prm, T, ctx_cap, q_start
+    def __init__(self, prm: Params, T: int, ctx_cap: int, q_start: int = 0, device="cuda", chunk_rows: int = 4096,
+                 with_lse: bool = False):
+        self.prm, self.T, self.ctx_cap, self.q_start, self.chunk_rows = prm, T, ctx_cap, q_start, chunk_rows
         G, H, D, P = prm.num_kv_groups, prm.num_kv_groups * prm.heads_per_group, prm.head_dim, prm.proxy_dim
-        B, k = prm.block_size, prm.top_k_blocks
-        self.R = max(B, min(T, chunk_rows) // B * B)  # rows per chunk, a multiple of B
+        B = prm.block_size
         mk = lambda *s: torch.empty(s, dtype=BF16, device=device)
-        self.d = dict(q=mk(T, H, D), k=mk(G, ctx_cap, D), v=mk(G, ctx_cap, D), gate=mk(T, H, D),
-                      k_proxy=mk(G, ctx_cap, P))
-        # q_proxy per chunk, contiguous [G, rows, P]; two buffers so that chunk j+1's copy
-        # overlaps chunk j's call
-        self.qp = [torch.empty(G * self.R * P, dtype=BF16, device=device) for _ in range(2)]
-        self.k_blk = torch.zeros((G, (ctx_cap + B - 1) // B, P), dtype=BF16, device=device)
-        self.sel = torch.empty(G * self.R * k, dtype=I32, device=device)
-        self.cnt = torch.empty(G * self.R, dtype=I32, device=device)
-        self.out = mk(T, H, D)
-        self.lse = torch.empty((T, H), dtype=F32, device=device)
-        self.ws = torch.empty(sgqa_workspace_bytes(prm, SGQA_OP_PREFILL, self.R, q_start + T), dtype=torch.uint8,
-                              device=device)
+        gate_shape = (T, H, D) if prm.gate_per_dim else (T, H)
+        self.d = dict(q=mk(T, H, D), k=mk(G, ctx_cap, D), v=mk(G, ctx_cap, D), gate=mk(*gate_shape),
+                      k_proxy=mk(G, ctx_cap, P), out=mk(T, H, D),
+                      k_blk=torch.zeros((G, (ctx_cap + B - 1) // B, P), dtype=BF16, device=device),
+                      lse=torch.empty((T, H), dtype=F32, device=device) if with_lse else None)
+        need = sgqa_workspace_bytes(prm, SGQA_OP_PREFILL_HOST, T, q_start + T, chunk_rows)
+        if need == 0:
+            raise ValueError("invalid prefill shape")
+        self.d["ws"] = torch.empty(need, dtype=torch.uint8, device=device)
         self.out_host = torch.empty((T, H, D), dtype=BF16, pin_memory=True)
-        self.s_in = torch.cuda.Stream(device)
-        self.s_out = torch.cuda.Stream(device)
+        self.lse_host = torch.empty((T, H), dtype=F32, pin_memory=True) if with_lse else None
 
     def h2d_bytes(self) -> int:
-        G, P = self.prm.num_kv_groups, self.prm.proxy_dim
-        return sum(t.numel() * t.element_size() for t in self.d.values()) + G * self.T * P * 2
+        G, P, D = self.prm.num_kv_groups, self.prm.proxy_dim, self.prm.head_dim
+        ctx = self.q_start + self.T  # cache positions read
+        rows = self.d["q"].numel() * 2 + self.d["gate"].numel() * 2 + G * self.T * P * 2
+        return rows + G * ctx * (2 * D + P) * 2
 
     def d2h_bytes(self) -> int:
-        return self.out_host.numel() * self.out_host.element_size()
+        n = self.out_host.numel() * self.out_host.element_size()
+        return n + (self.lse_host.numel() * 4 if self.lse_host is not None else 0)
 
     def run(self, host: dict, stream=None) -> torch.Tensor:
-        prm, d, R, q0 = self.prm, self.d, self.R, self.q_start
-        G, P, k = prm.num_kv_groups, prm.proxy_dim, prm.top_k_blocks
-        comp = stream if stream is not None else torch.cuda.current_stream()
-        begin = torch.cuda.Event()
-        begin.record(comp)
-        self.s_in.wait_event(begin)
-        self.s_out.wait_event(begin)
-        released = []  # per chunk: its layer call has finished (its q_proxy buffer is free)
-        ctx_done = 0   # cache positions copied so far
-        for j, a in enumerate(range(0, self.T, R)):
-            b = min(self.T, a + R)
-            rows = b - a
-            qp = self.qp[j % 2][:G * rows * P].view(G, rows, P)
-            with torch.cuda.stream(self.s_in):
-                if j >= 2:
-                    self.s_in.wait_event(released[j - 2])
-                hi = q0 + b  # cache positions this chunk attends to
-                for name in ("k", "v", "k_proxy"):
-                    for g in range(G):
-                        d[name][g, ctx_done:hi].copy_(host[name][g, ctx_done:hi], non_blocking=True)
-                d["q"][a:b].copy_(host["q"][a:b], non_blocking=True)
-                d["gate"][a:b].copy_(host["gate"][a:b], non_blocking=True)
-                for g in range(G):
-                    qp[g].copy_(host["q_proxy"][g, a:b], non_blocking=True)
-                copied = torch.cuda.Event()
-                copied.record(self.s_in)
-            comp.wait_event(copied)
-            if j == 0 and q0 > 0:  # blocks of the cached prefix
-                sgqa_build_block_index(prm, d["k_proxy"], 0, q0, self.k_blk, comp)
-            sgqa_prefill(prm, d["q"][a:b], d["k"], d["v"], d["gate"][a:b], qp, d["k_proxy"], q0 + a, self.k_blk,
-                         self.sel[:G * rows * k].view(G, rows, k), self.cnt[:G * rows].view(G, rows), self.out[a:b],
-                         self.lse[a:b], self.ws, comp)
-            done = torch.cuda.Event()
-            done.record(comp)
-            released.append(done)
-            ctx_done = hi
-            self.s_out.wait_event(done)
-            with torch.cuda.stream(self.s_out):
-                self.out_host[a:b].copy_(self.out[a:b], non_blocking=True)
-        end = torch.cuda.Event()
-        end.record(self.s_out)
-        comp.wait_event(end)
+        h = dict(host, out=self.out_host)
+        if self.lse_host is not None:
+            h["lse"] = self.lse_host
+        sgqa_prefill_host(self.prm, h, self.d, self.q_start, self.chunk_rows, stream)
         return self.out_host
-

@@ -49,7 +49,7 @@ extern "C" {
 /* The stream type of the CUDA runtime (cudaStream_t); 0 is the legacy default stream. */
 typedef struct CUstream_st* sgqa_stream_t;
 
-#define SGQA_ABI_VERSION 1
+#define SGQA_ABI_VERSION 2
 
 typedef enum {
   SGQA_OK = 0,
@@ -70,10 +70,19 @@ typedef struct {
   int32_t top_k_blocks;     /* k >= 1 (512 on the pages = 4,096 tokens) */
   int32_t gate_per_dim;     /* 1: gate is [T, H, D] (element-wise); 0: gate is [T, H] (per head) */
   float softmax_scale;      /* scale on q.k; <= 0 selects 1/sqrt(D) */
+  int32_t attn_kernel;      /* prefill attention kernel: SGQA_ATTN_AUTO (0, the default), or
+                               SGQA_ATTN_WARP / SGQA_ATTN_TC_UNION to force one (see
+                               sgqa_attention_kernel); other values are INVALID_ARGUMENT */
 } sgqa_params;
 
+/* Prefill attention kernels (sgqa_params.attn_kernel, sgqa_attention_kernel()). */
+#define SGQA_ATTN_AUTO 0      /* the union kernel where its shape holds, else the warp-level one */
+#define SGQA_ATTN_WARP 1      /* one warp per (row, group) on warp-level MMAs: every shape */
+#define SGQA_ATTN_TC_UNION 2  /* 8 query rows per unit over the union of their selected blocks,
+                                 tcgen05 with the (row, head) pairs as the MMA's M */
+
 /* Operation selector for sgqa_workspace_bytes(). */
-enum { SGQA_OP_INDEX_TOPK = 1, SGQA_OP_PREFILL = 2, SGQA_OP_DECODE = 3, SGQA_OP_ATTN = 4 };
+enum { SGQA_OP_INDEX_TOPK = 1, SGQA_OP_PREFILL = 2, SGQA_OP_DECODE = 3, SGQA_OP_ATTN = 4, SGQA_OP_PREFILL_HOST = 5 };
 
 /* ---------------------------------------------------------------------------------
  * Block index (ai4snews item, Interpretation para 2: "compresses indexers for adjacent
@@ -160,6 +169,65 @@ SGQA_API sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const v
                          sgqa_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * End-to-end prefill from HOST memory: the same layer as sgqa_prefill (same passages),
+ * with the host-to-device copies of the inputs and the device-to-host copy of the output
+ * inside the call.  The query rows are processed in chunks of `chunk_rows` (a multiple of
+ * B; <= 0 selects 4,096).  Chunk j needs the caches up to its last position only
+ * (causality), so its copy-in, its prefill (a chunked prefill at q_start + its first row)
+ * and its copy-out run on three streams and overlap with the neighbouring chunks: the
+ * library copies in on one stream of its own, computes on `stream` and copies out on a
+ * second stream of its own.  Outputs are bit-identical to one sgqa_prefill over all rows.
+ *
+ * Host tensors (pinned memory for overlapped copies; pageable memory works but the
+ * copies then serialise with the host):
+ *   q, gate [T, H, D] (gate [T, H] when gate_per_dim = 0); q_proxy [G, T, P];
+ *   k, v [G, ctx_cap, D] and k_proxy [G, ctx_cap, P]: positions [0, q_start + T) are read
+ *   (a cached prefix [0, q_start) is copied too and its blocks are built on the device);
+ *   out [T, H, D] bf16 written; lse [T, H] fp32 written when not NULL.
+ * Device tensors (caller-owned, same layouts; they hold the inputs and outputs afterwards):
+ *   q, gate, out [T, ...]; k, v, k_proxy [G, ctx_cap, ...]; k_blk [G, nb_cap, P];
+ *   lse [T, H] (required when host lse is given; may be NULL otherwise);
+ *   ws >= sgqa_workspace_bytes(prm, SGQA_OP_PREFILL_HOST, T, q_start + T, chunk_rows),
+ *   16-byte aligned: two q_proxy chunk buffers, the chunk's selection and the indexer
+ *   workspace are carved from it.
+ * Ordering: all work is ordered after what `stream` had enqueued before the call, and
+ * `stream` waits for the last copy-out, so an event recorded on `stream` after the call
+ * completes with the whole job (synchronise `stream` before reading host out / lse).
+ * The first call on a device creates two non-blocking streams and ten events, kept until
+ * the process exits; calls on one device enqueue one at a time (a mutex).  No device
+ * memory is allocated.  Errors: as sgqa_prefill, checked before anything is enqueued; a
+ * failed CUDA call while enqueuing returns SGQA_ERR_CUDA.
+ * ------------------------------------------------------------------------------- */
+typedef struct {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* gate;
+  const void* q_proxy;
+  const void* k_proxy;
+  void* out;
+  float* lse;
+} sgqa_host_tensors;
+
+typedef struct {
+  void* q;
+  void* k;
+  void* v;
+  void* gate;
+  void* k_proxy;
+  void* k_blk;
+  int64_t nb_cap;
+  void* out;
+  float* lse;
+  void* ws;
+  size_t ws_bytes;
+} sgqa_device_tensors;
+
+SGQA_API sgqa_status sgqa_prefill_host(const sgqa_params* prm, const sgqa_host_tensors* host,
+                                       const sgqa_device_tensors* dev, int64_t ctx_cap, int64_t T, int64_t q_start,
+                                       int64_t chunk_rows, sgqa_stream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * Decode step for `batch` sequences packed in shared caches.  Sequence s occupies cache
  * rows [kv_off[s], kv_off[s] + ctx_len[s]); kv_off[s] is a multiple of B.  Its new
  * query sits at position ctx_len[s]-1 and its K, V and proxy key are already in the
@@ -233,7 +301,8 @@ SGQA_API sgqa_status sgqa_decode_fp8(const sgqa_params* prm, int32_t batch, cons
                                      void* out, float* lse, void* ws, size_t ws_bytes, sgqa_stream_t stream);
 
 /* Workspace bytes needed by `op` for T query rows ending at context length ctx_len
- * (decode: the largest ctx_len of the batch).  Returns 0 for an invalid request. */
+ * (decode: the largest ctx_len of the batch; SGQA_OP_PREFILL_HOST: `batch` carries the
+ * call's chunk_rows, <= 0 for the default).  Returns 0 for an invalid request. */
 SGQA_API size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64_t ctx_len, int32_t batch);
 
 /* Synchronizes `stream`, then returns and clears the current device's sticky device
@@ -253,16 +322,13 @@ SGQA_API sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns);
 SGQA_API sgqa_status sgqa_selftest_wait_timeout(uint64_t limit_ns, sgqa_stream_t stream);
 
 /* Which attention kernel sgqa_sparse_attn_fwd / sgqa_prefill launch for these arguments
- * (no launch, no device access): SGQA_ATTN_WARP = one warp per (row, group) on warp-level
- * MMAs; SGQA_ATTN_TC_ROW = one (row, group) per CTA on tcgen05, keys as the MMA's M (opt-in,
- * environment SGQA_K4_IMPL=tc); SGQA_ATTN_TC_UNION = 8 query rows per unit over the union of
- * their selected blocks on tcgen05, the default whenever its shape holds (blocks of 8, 16
- * heads per group, top_k_blocks <= 512, block indices below 65,536, not dense_mode);
- * SGQA_ATTN_WARP otherwise.  SGQA_K4_IMPL=mma|tc|union, read once per process, overrides
- * the choice where the arguments allow it.  Returns -1 for invalid parameters. */
-#define SGQA_ATTN_WARP 0
-#define SGQA_ATTN_TC_ROW 1
-#define SGQA_ATTN_TC_UNION 2
+ * (no launch, no device access).  With prm->attn_kernel = SGQA_ATTN_AUTO: SGQA_ATTN_TC_UNION
+ * whenever its shape holds (blocks of 8, 16 heads per group, top_k_blocks <= 512, every
+ * block index of the call below 2^17, i.e. positions below 1,048,576, not dense_mode),
+ * SGQA_ATTN_WARP otherwise.  A forced kernel is returned when it can serve the call; a
+ * forced SGQA_ATTN_TC_UNION outside its shape returns -1, and the attention entries then
+ * fail with SGQA_ERR_UNSUPPORTED_SHAPE.  Returns -1 for invalid parameters.  Decode always
+ * runs the warp-level kernel (split over the context). */
 SGQA_API int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode);
 
 /* Short English description of a status code (static storage). */

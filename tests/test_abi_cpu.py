@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_abi_version(lib):
-    assert lib.abi_version() == 1
+    assert lib.abi_version() == 2
 
 
 def test_status_strings(lib):
@@ -105,3 +105,52 @@ def test_workspace_sizes(lib):
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 8) > 0
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 0) == 0
     assert lib.sgqa_workspace_bytes(lib.params(B=3), lib.SGQA_OP_PREFILL, 16, 16) == 0
+
+
+def test_attention_kernel_choice(lib):
+    """Which prefill attention kernel a call launches (no device access): the union kernel
+    wherever its shape holds, up to the 1M-token context; the warp-level kernel for other
+    shapes, dense mode and when forced; -1 for a forced union outside its shape."""
+    auto = lib.params()
+    assert lib.sgqa_attention_kernel(auto, 131072, 0) == lib.ATTN_TC_UNION
+    assert lib.sgqa_attention_kernel(auto, 8192, 1040384) == lib.ATTN_TC_UNION   # the 1M chunk
+    assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8192) == lib.ATTN_TC_UNION
+    assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8191) == lib.ATTN_WARP  # past 2^18 blocks
+    assert lib.sgqa_attention_kernel(auto, 1024, 0, dense_mode=True) == lib.ATTN_WARP
+    assert lib.sgqa_attention_kernel(lib.params(B=4, k=1024), 1024, 0) == lib.ATTN_WARP
+    assert lib.sgqa_attention_kernel(lib.params(Hg=8), 1024, 0) == lib.ATTN_WARP
+    assert lib.sgqa_attention_kernel(lib.params(k=513), 1024, 0) == lib.ATTN_WARP
+    warp = lib.params(attn_kernel=lib.ATTN_WARP)
+    assert lib.sgqa_attention_kernel(warp, 131072, 0) == lib.ATTN_WARP
+    union = lib.params(attn_kernel=lib.ATTN_TC_UNION)
+    assert lib.sgqa_attention_kernel(union, 131072, 0) == lib.ATTN_TC_UNION
+    assert lib.sgqa_attention_kernel(lib.params(B=16, k=256, attn_kernel=lib.ATTN_TC_UNION), 1024, 0) == -1
+    assert lib.sgqa_attention_kernel(union, 1024, 0, dense_mode=True) == -1
+    assert lib.sgqa_attention_kernel(lib.params(attn_kernel=7), 1024, 0) == -1
+
+
+def test_forced_union_outside_its_shape_is_rejected(lib):
+    prm = lib.params(B=16, k=256, attn_kernel=lib.ATTN_TC_UNION)
+    a = ctypes.c_void_p(1 << 12)
+    f = lib._lib.sgqa_sparse_attn_fwd
+    assert f(ctypes.byref(prm), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None) == 2
+    assert f(ctypes.byref(lib.params(attn_kernel=3)), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None) == 1
+
+
+def test_prefill_host_validation(lib):
+    prm = lib.params(G=1, Hg=16, k=8)
+    a = 1 << 12
+    ht = lib.HostTensors(a, a, a, a, a, a, a, None)
+    ws_need = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL_HOST, 1000, 1000, 256)
+    assert ws_need > 0
+    dt = lambda ws_bytes, lse=None, nb=125: lib.DeviceTensors(a, a, a, a, a, a, nb, a, lse, a, ws_bytes)
+    f = lambda h, d, T=1000, q0=0, cap=1000, chunk=256: lib._lib.sgqa_prefill_host(
+        ctypes.byref(prm), ctypes.byref(h), ctypes.byref(d), cap, T, q0, chunk, None)
+    assert f(ht, dt(ws_need - 1)) == 3                       # workspace too small
+    assert f(ht, dt(ws_need), T=1001) == 1                   # rows past the cache
+    assert f(ht, dt(ws_need, nb=124)) == 1                   # blocks beyond nb_cap
+    assert f(lib.HostTensors(a, a, a, a, a, a, None, None), dt(ws_need)) == 1   # no host output
+    assert f(lib.HostTensors(a, a, a, a, a, a, a, a), dt(ws_need)) == 1         # host lse without device lse
+    assert f(ht, dt(ws_need), T=0) == 0                      # nothing to do
+    # the chunk size moves the workspace: two q_proxy chunks, the chunk's selection, one indexer pass
+    assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL_HOST, 1000, 1000, 512) > ws_need

@@ -223,21 +223,54 @@ def test_small_workspace_many_passes(sg):
     assert torch.equal(idx, res.sel_idx) and torch.equal(cnt, res.sel_cnt)
 
 
-@pytest.mark.parametrize("q_start", [0, 1000])
-def test_host_prefill_pipeline_equals_device_prefill(sg, q_start):
-    """The end-to-end API (pinned host tensors, chunks of rows pipelined over three
-    streams) gives bit-identical outputs to one prefill call on device tensors."""
+@pytest.mark.parametrize("q_start,gate_per_dim", [(0, 1), (1000, 1), (1000, 0)])
+def test_host_prefill_pipeline_equals_device_prefill(sg, q_start, gate_per_dim):
+    """The end-to-end entry sgqa_prefill_host (pinned host tensors, chunks of rows
+    pipelined by the library over its copy-in stream, the calling stream and its copy-out
+    stream) gives bit-identical outputs and LSE to one prefill call on device tensors."""
     wl = gen.small_workload(T=2600, G=2, Hg=16, B=8, k=24, planted=True, q_start=q_start)
     inp = _to_cuda(gen.make_inputs(wl, seed=11))
-    prm = _prm(sg, wl)
-    res = _gpu_prefill(sg, inp, wl, prm)
-    hp = sg.HostPrefill(prm, wl.T, wl.C, wl.q_start, chunk_rows=1024)  # three chunks
-    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "gate", "q_proxy", "k_proxy")}
+    prm = _prm(sg, wl, gate_per_dim=gate_per_dim)
+    gate = inp.gate if gate_per_dim else inp.gate[:, :, 0].contiguous()
+    res = _gpu_prefill(sg, inp, wl, prm, gate=gate)
+    hp = sg.HostPrefill(prm, wl.T, wl.C, wl.q_start, chunk_rows=1024, with_lse=True)  # three chunks
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "q_proxy", "k_proxy")}
+    host["gate"] = gate.cpu().pin_memory()
     for _ in range(2):  # a second run reuses every buffer
+        hp.out_host.zero_()
         out = hp.run(host)
         torch.cuda.synchronize()
         assert sg.sgqa_get_device_error() == 0
         assert torch.equal(out, res.out.cpu())
+        assert torch.equal(hp.lse_host, res.lse.cpu())
+        assert torch.equal(hp.d["k_blk"], res.k_blk)
+
+
+def test_block_index_real_valued_proxies_within_one_ulp(sg):
+    """The block mean on arbitrary (non-integer) proxies: the device sums the 8 bf16 token
+    proxies in fp32 and rounds once, the oracle takes the fp64 mean and rounds once.  They
+    agree exactly unless the fp32 sum itself rounded, and then by at most one bf16 ulp.
+    Proxies N(0,1) times 2^e, e uniform in [-12, 11] per token, so most 8-term sums span
+    more than 24 bits; the last block is partial (the fp64 division path)."""
+    G, C, P, B = 2, 8192 + 5, 256, 8
+    g = torch.Generator().manual_seed(31)
+    scale = torch.exp2(torch.randint(-12, 12, (G, C, 1), generator=g).float())
+    kp = (torch.randn((G, C, P), generator=g) * scale).to(torch.bfloat16)
+    prm = sg.params(G=G, Hg=16, P=P, B=B, k=8)
+    nb = (C + B - 1) // B
+    kb = torch.zeros((G, nb, P), dtype=torch.bfloat16, device="cuda")
+    sg.sgqa_build_block_index(prm, kp.cuda(), 0, C, kb)
+    torch.cuda.synchronize()
+    assert sg.sgqa_get_device_error() == 0
+    ref = oracle.block_index(u16(kp), B, 0, C).astype(np.int32)
+    got = u16(kb).astype(np.int32)
+    # bf16 payloads as ordered integers: adjacent representable values differ by one
+    mono = lambda x: np.where(x & 0x8000, -(x & 0x7FFF), x & 0x7FFF)
+    dist = np.abs(mono(got) - mono(ref))
+    assert dist.max() <= 1, f"block index more than one bf16 ulp from the fp64 mean ({dist.max()})"
+    same = float((dist == 0).mean())
+    print(f"bit-identical block proxies: {same:.6f} of {dist.size}")
+    assert same > 0.9
 
 
 # ---------------------------------------------------------------------------------------
@@ -291,7 +324,7 @@ def test_l128k_sampled_rows(sg):
     wl = gen.WORKLOADS["l128k"]
     inp = gen.make_inputs(wl, seed=0, device="cuda")
     res = _gpu_prefill(sg, inp, wl, _prm(sg, wl))
-    rows = sample_rows(wl.T, 256, seed=1, B=wl.B, k=wl.k)
+    rows = sample_rows(wl.T, 1024, seed=1, B=wl.B, k=wl.k)
     _check_prefill(inp, wl, res, rows)
     del inp, res
     gc.collect()
