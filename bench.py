@@ -37,7 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline per stage"
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
-K4_KERNEL = {1: "k4_sparse_attn", 2: "k4u_sparse_attn"}
+K4_KERNEL = {1: "k4_sparse_attn", 2: "k4u_sparse_attn", 3: "k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn"}
 
 
 def load_peaks():
@@ -91,23 +91,36 @@ def selection_stats(plan, wl, units_per_pass=4096):
     G, T, k = sel.shape
     nb = (wl.q_start + wl.T + wl.B - 1) // wl.B
     used = torch.zeros((G, nb + 1), dtype=torch.bool, device=sel.device)
-    chunks = 0
+    chunks = r_chunks = r_stages = r_union = r_warp = 0
     blocks = 0
     units = sel.view(G, T // 8, 8 * k)
+    cnt = plan.sel_cnt.view(G, T // 8, 8).sum(dim=-1)  # (row, block) pairs per unit
     for u0 in range(0, T // 8, units_per_pass):
         part = units[:, u0:u0 + units_per_pass]
         srt, _ = torch.sort(part, dim=-1)
         valid = srt >= 0
         new = valid.clone()
         new[..., 1:] &= srt[..., 1:] != srt[..., :-1]
-        nu = new.sum(dim=-1)  # [G, units]
+        nu = new.sum(dim=-1)  # [G, units]: distinct blocks
+        pairs = cnt[:, u0:u0 + units_per_pass]
+        # the library's routing rule: union iff 100 * windows * |union| <= 55 * pairs, windows
+        # = the 16,384-block windows the unit's own blocks reach
+        last_row = torch.clamp(torch.arange(u0, u0 + pairs.shape[1], device=sel.device) * 8 + 7, max=T - 1)
+        windows = (wl.q_start + last_row) // wl.B // 16384 + 1
+        to_union = 100 * windows[None, :] * nu <= 55 * pairs
         blocks += int(nu.sum())
         chunks += int(((nu + 15) // 16).sum())
+        r_chunks += int(((nu + 15) // 16)[to_union].sum())
+        r_stages += int(((plan.sel_cnt.view(G, T // 8, 8)[:, u0:u0 + units_per_pass] + 1) // 2)[~to_union].sum())
+        r_union += int(to_union.sum())
+        r_warp += int((~to_union).sum())
         for g in range(G):
             used[g].index_fill_(0, (srt[g][valid[g]]).long(), True)
         del srt, valid, new
+    n_units = G * (T // 8)
     return {"kv_blocks_selected": int(used.sum()), "union_chunks": chunks,
-            "union_mean_blocks": round(blocks / (G * (T // 8)), 1)}
+            "union_mean_blocks": round(blocks / n_units, 1), "routed_union_chunks": r_chunks,
+            "routed_warp_stages": r_stages, "routed_union_units": r_union, "routed_warp_units": r_warp}
 
 
 def cpu_model() -> str:
@@ -340,7 +353,7 @@ def run_sgqa(args, rank, world, local_rank):
         if evs:
             evs[2].record(stream)
         sgqa.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, plan.sel_idx, plan.sel_cnt, wl.q_start,
-                                  plan.out, plan.lse, stream=stream)
+                                  plan.out, plan.lse, stream=stream, ws=plan.ws)
         if evs:
             evs[3].record(stream)
 
@@ -411,7 +424,18 @@ def run_sgqa(args, rank, world, local_rank):
     k4s["per_row_gather_bytes"] = w["k4_gather_bytes"] + w["k4_rows_bytes"]
     k4s["per_row_gather_frac_of_hbm"] = round(k4s["per_row_gather_bytes"] / (k4_ms / 1e3) / hbm_bps, 4)
     k4_kernel = K4_KERNEL.get(sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start), "k4_sparse_attn")
-    if sel_stats is not None and k4_kernel == "k4u_sparse_attn":
+    if sel_stats is not None and k4_kernel.startswith("k4r_count"):
+        # routed: units whose union is small go to the union kernel, the rest to the
+        # warp-level kernel (16 heads x 16 keys x 192 x 4 per stage of two blocks)
+        issued = (sel_stats["routed_union_chunks"] * 128 * 128 * wl.D * 4
+                  + sel_stats["routed_warp_stages"] * 16 * 16 * wl.D * 4)
+        k4s["union_mean_blocks"] = sel_stats["union_mean_blocks"]
+        k4s["units_to_union_kernel"] = sel_stats["routed_union_units"]
+        k4s["units_to_warp_kernel"] = sel_stats["routed_warp_units"]
+        k4s["issued_mma_tflop"] = round(issued / 1e12, 3)
+        k4s["issued_tflops"] = round(issued / (k4_ms / 1e3) / 1e12, 2)
+        k4s["useful_share_of_issued"] = round(w["k4_flop"] / issued, 4)
+    elif sel_stats is not None and k4_kernel == "k4u_sparse_attn":
         issued = sel_stats["union_chunks"] * 128 * 128 * wl.D * 4
         k4s["union_mean_blocks"] = sel_stats["union_mean_blocks"]
         k4s["issued_mma_tflop"] = round(issued / 1e12, 3)

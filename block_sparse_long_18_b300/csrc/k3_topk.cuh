@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   if (!STREAM) load_tile(0);
 
   // Slots past the last candidate hold key 0.  Every finite score maps to a key of at
-  // least 0x007FFFFF (the key of -inf), so key 0 only ever lands in bin 0 of the first
-  // digit, below every real candidate; since there are more candidates than keys to keep,
-  // the search never reaches it and no pass needs an index test.
+  // least 0x007FFFFF (the key of -inf), so key 0 lies below every real candidate; the first
+  // pass does not count it, and since there are more candidates than keys to keep, the
+  // search never reaches it and no later pass needs an index test.
   for (int b = tid; b < NBINS; b += NT) {
     hist2[0][b] = 0;
     hist2[1][b] = 0;
@@ -231,7 +231,8 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
 #pragma unroll
       for (int q = 0; q < PER; ++q) {
         const uint32_t kk = key[q];
-        if (p == 0 || (kk & pmask) == prefix) atomicAdd(&hist[(kk >> sh) & wm], 1u);
+        // pass 0 skips the empty slots (key 0): they would all hit one bin
+        if (p == 0 ? kk != 0u : (kk & pmask) == prefix) atomicAdd(&hist[(kk >> sh) & wm], 1u);
       }
     }
     __syncthreads();  // (1) histogram complete
@@ -296,9 +297,10 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
       }
     }
     __syncthreads();
-    uint32_t w = bitmap[tid];
+    constexpr int NWORDS = NT * PER / 32;  // bitmap words; thread tid reads word tid
+    uint32_t w = tid < NWORDS ? bitmap[tid] : 0u;
     if (skip != 0u) {  // block-uniform
-      uint32_t wt = tiemap[tid], ttot;
+      uint32_t wt = tid < NWORDS ? tiemap[tid] : 0u, ttot;
       uint32_t rank = k3_block_excl_scan<NT>((uint32_t)__popc(wt), warp_tot, ttot);  // ties before this word
       while (wt != 0u) {
         const uint32_t bit = wt & (0u - wt);

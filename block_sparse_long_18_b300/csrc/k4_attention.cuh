@@ -59,6 +59,10 @@ struct K4Args {
   int32_t gate_per_dim;
   int32_t nsplit;
   int32_t use_pos;
+  // routed mode (nsplit = 1, NW = 8): CTA b serves the 8-row unit units[b] (unit = g * tiles
+  // + tile of 8 rows), one warp per row, for b < *n_units_dev
+  const int32_t* units;
+  const int32_t* n_units_dev;
   uint64_t wait_ns;
   int64_t pos[256];
   int64_t kv_off[256];
@@ -94,7 +98,16 @@ __global__ void __launch_bounds__(NW * 32, 1)
   const uint32_t bar0 = smem_u32(smem) + NW * NSTAGE * K4_STAGE + warp * NSTAGE * 8;
 
   const int64_t n_units = (int64_t)a.G * a.rows * a.nsplit;
-  const int64_t unit = (int64_t)blockIdx.x * NW + warp;
+  int64_t unit = (int64_t)blockIdx.x * NW + warp;
+  if (a.units) {
+    static_assert(NW == 8, "a routed unit is 8 rows, one per warp");
+    if ((int64_t)blockIdx.x >= (int64_t)*a.n_units_dev) return;
+    const int64_t ntiles = (a.rows + 7) / 8;
+    const int64_t uid = __ldg(a.units + blockIdx.x);
+    const int64_t row = (uid % ntiles) * 8 + warp;
+    if (row >= a.rows) return;
+    unit = (uid / ntiles) * a.rows + row;
+  }
   if (unit >= n_units) return;
   const int32_t split = (int32_t)(unit % a.nsplit);
   const int64_t gr = unit / a.nsplit;
@@ -494,7 +507,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
 }
 
-// Merge split-K partials: one warp per (row, group, head).
+// Merge split-K partials.  One warp per (row, group, head, 32-wide slice of D): lane s
+// reads split s's (m, l) to form the weights, then lane d sums its column over the splits
+// with every split's load issued at once (the partials sit in L2; a warp that walked the
+// splits one after another would wait on each load in turn).
 struct K4CombineArgs {
   const float* part_o;     // [G*rows*nsplit, 16, D]
   const float* part_ml;    // [G*rows*nsplit, 16, 2]
@@ -504,21 +520,24 @@ struct K4CombineArgs {
   int64_t rows;
   int32_t G, Hg, H, nsplit, gate_per_dim;  // nsplit <= 32 (one lane per split)
 };
+constexpr int K4C_SLICES = K4_D / 32;  // warps per (row, group, head)
 
-__global__ void __launch_bounds__(256) k4_combine(const K4CombineArgs a) {
+__global__ void __launch_bounds__(128) k4_combine(const K4CombineArgs a) {
   const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const uint32_t lane = lane_id();
-  const int64_t total = (int64_t)a.G * a.rows * a.Hg;
+  const int64_t total = (int64_t)a.G * a.rows * a.Hg * K4C_SLICES;
   if (wid >= total) return;
-  const int h = (int)(wid % a.Hg);
-  const int64_t gr = wid / a.Hg;           // = g * rows + i
+  const int sl = (int)(wid % K4C_SLICES);
+  const int64_t gh = wid / K4C_SLICES;
+  const int h = (int)(gh % a.Hg);
+  const int64_t gr = gh / a.Hg;            // = g * rows + i
   const int g = (int)(gr / a.rows);
   const int64_t i = gr % a.rows;
   // lane s holds split s (nsplit <= 32): its (m, l), the maximum over splits with mass and
   // its weight exp2(m_s - M)
   float ms = -INFINITY, ls = 0.f;
   if ((int)lane < a.nsplit) {
-    const float2 ml = *reinterpret_cast<const float2*>(a.part_ml + ((gr * a.nsplit + lane) * 16 + h) * 2);
+    const float2 ml = __ldg(reinterpret_cast<const float2*>(a.part_ml + ((gr * a.nsplit + lane) * 16 + h) * 2));
     if (ml.y > 0.f) {
       ms = ml.x;
       ls = ml.y;
@@ -531,29 +550,23 @@ __global__ void __launch_bounds__(256) k4_combine(const K4CombineArgs a) {
   float L = ws * ls;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  // O: lane d-slice (d = lane + 32 e), summed over the splits with their weights
-  float acc[6] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const float* po = a.part_o + (gr * a.nsplit * 16 + h) * K4_D + lane;
-  // no branch on the weight: every split's loads can be in flight together (a split that
-  // got no keys wrote zero partials and has weight 0)
-#pragma unroll 8
-  for (int s = 0; s < a.nsplit; ++s) {
-    const float w = __shfl_sync(0xffffffffu, ws, s);
-    const float* ps = po + (int64_t)s * 16 * K4_D;
+  // column d = 32 sl + lane, summed over the splits (a split that got no keys wrote zero
+  // partials and has weight 0)
+  const int d = 32 * sl + (int)lane;
+  const float* po = a.part_o + (gr * a.nsplit * 16 + h) * K4_D + d;
+  float x[32];
 #pragma unroll
-    for (int e = 0; e < 6; ++e) acc[e] = fmaf(w, __ldg(ps + 32 * e), acc[e]);
-  }
+  for (int s = 0; s < 32; ++s) x[s] = s < a.nsplit ? __ldg(po + (int64_t)s * 16 * K4_D) : 0.f;
+  float acc = 0.f;
+#pragma unroll
+  for (int s = 0; s < 32; ++s) acc = fmaf(__shfl_sync(0xffffffffu, ws, s), x[s], acc);
   const float inv = L > 0.f ? __frcp_rn(L) : 0.f;
   const int64_t head = i * a.H + (int64_t)g * a.Hg + h;
   const float kLog2e = 1.4426950408889634f;
-#pragma unroll
-  for (int e = 0; e < 6; ++e) {
-    const int d = lane + 32 * e;
-    const float gv = a.gate_per_dim ? __bfloat162float(a.gate[head * K4_D + d]) : __bfloat162float(a.gate[head]);
-    const float sg = __frcp_rn(1.f + fast_exp2(-gv * kLog2e));
-    a.out[head * K4_D + d] = __float2bfloat16_rn(acc[e] * inv * sg);
-  }
-  if (a.lse && lane == 0) a.lse[head] = (M + __log2f(L)) * 0.6931471805599453f;
+  const float gv = a.gate_per_dim ? __bfloat162float(a.gate[head * K4_D + d]) : __bfloat162float(a.gate[head]);
+  const float sg = __frcp_rn(1.f + fast_exp2(-gv * kLog2e));
+  a.out[head * K4_D + d] = __float2bfloat16_rn(acc * inv * sg);
+  if (a.lse && sl == 0 && lane == 0) a.lse[head] = (M + __log2f(L)) * 0.6931471805599453f;
 }
 
 }  // namespace sgqa

@@ -58,8 +58,8 @@ constexpr uint32_t K4U_V_OFF = 2 * K4U_SLOT;
 constexpr uint32_t K4U_T_OFF = 4 * K4U_SLOT;
 constexpr uint32_t K4U_BM_OFF = K4U_T_OFF + 2 * K4U_TB;      // uint32 [K4U_WIN / 32] window bitmap
 constexpr uint32_t K4U_PRE_OFF = K4U_BM_OFF + K4U_WIN / 8;   // uint32 [K4U_WIN / 32] prefix counts
-constexpr uint32_t K4U_X_OFF = K4U_PRE_OFF + K4U_WIN / 8;    // float [128]: row sums per (row, head) pair
-constexpr uint32_t K4U_BAR_OFF = K4U_X_OFF + 128 * 4;
+constexpr uint32_t K4U_X_OFF = K4U_PRE_OFF + K4U_WIN / 8;    // float [2][128]: row sums, reference maxima per pair
+constexpr uint32_t K4U_BAR_OFF = K4U_X_OFF + 2 * 128 * 4;
 constexpr uint32_t K4U_SMEM = K4U_BAR_OFF + 512 + 1024;     // + barriers, flags, alignment
 constexpr int K4U_THREADS = 384;
 constexpr uint32_t kSuspendNs = 20000;  // a waiting role sleeps in its polls (woken when the phase completes)
@@ -78,6 +78,10 @@ struct K4UArgs {
   float scale_log2;
   int32_t gate_per_dim;
   uint64_t wait_ns;
+  // routed mode: the units to serve are units[0 .. *n_units_dev) (unit = g * tiles + tile
+  // of 8 rows); otherwise every unit of the call
+  const int32_t* units;
+  const int32_t* n_units_dev;
 };
 
 __global__ void __launch_bounds__(K4U_THREADS, 1)
@@ -96,7 +100,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
   const int64_t ntiles = (a.rows + 7) / 8;
-  const int64_t n_units = (int64_t)a.G * ntiles;
+  // units of this launch: every (group, 8-row tile), or the routed list
+  const int64_t n_units = a.units ? (int64_t)*a.n_units_dev : (int64_t)a.G * ntiles;
+  auto unit_id = [&](int64_t u) -> int64_t { return a.units ? (int64_t)__ldg(a.units + u) : u; };
   auto tbl = [&](uint32_t buf) { return smem + K4U_T_OFF + buf * K4U_TB; };
 
   if (threadIdx.x == 0) {
@@ -148,8 +154,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     for (int64_t u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
       const uint32_t buf = uc & 1;
       if (uc >= 2 && !warp_wait(kTblEmpty + buf, ((uc >> 1) - 1) & 1)) break;
-      const int32_t g = (int32_t)(u / ntiles);
-      const int64_t i0 = (u % ntiles) * 8;
+      const int64_t uid = unit_id(u);
+      const int32_t g = (int32_t)(uid / ntiles);
+      const int64_t i0 = (uid % ntiles) * 8;
       uint8_t* T = tbl(buf);
       uint16_t* ublk = reinterpret_cast<uint16_t*>(T + K4U_TB_UBLK);
       uint32_t* rbits = reinterpret_cast<uint32_t*>(T + K4U_TB_RBITS);
@@ -292,7 +299,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
       const uint32_t buf = uc & 1;
       if (!warp_wait(kTblFull + buf, (uc >> 1) & 1)) break;
-      const int32_t g = (int32_t)(u / ntiles);
+      const int32_t g = (int32_t)(unit_id(u) / ntiles);
       const uint8_t* T = tbl(buf);
       const uint16_t* ublk = reinterpret_cast<const uint16_t*>(T + K4U_TB_UBLK);
       const int32_t* meta = reinterpret_cast<const int32_t*>(T + K4U_TB_META);
@@ -414,8 +421,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     constexpr float kLazy = 8.f;  // reference maximum refreshed only past 2^8
 
     auto write_q = [&](int64_t u) {  // this half of the Q rows of unit u -> tensor memory
-      const int32_t g = (int32_t)(u / ntiles);
-      const int64_t i = (u % ntiles) * 8 + r;
+      const int64_t uid = unit_id(u);
+      const int32_t g = (int32_t)(uid / ntiles);
+      const int64_t i = (uid % ntiles) * 8 + r;
       const bool valid = i < a.rows;
       const uint4* src =
           reinterpret_cast<const uint4*>(a.q + ((i * a.H) + (int64_t)g * 16 + h) * K4U_D + 96 * hf);
@@ -471,8 +479,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       const uint32_t buf = uc & 1;
       wait_ok(kTblFull + buf, (uc >> 1) & 1);
       if (sync_stop()) break;
-      const int32_t g = (int32_t)(u / ntiles);
-      const int64_t i = (u % ntiles) * 8 + r;
+      const int64_t uid = unit_id(u);
+      const int32_t g = (int32_t)(uid / ntiles);
+      const int64_t i = (uid % ntiles) * 8 + r;
       const bool row_ok = i < a.rows;
       const uint8_t* T = tbl(buf);
       const uint32_t* rb = reinterpret_cast<const uint32_t*>(T + K4U_TB_RBITS);
@@ -485,10 +494,11 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(gp));
         asm volatile("prefetch.global.L2 [%0];" ::"l"(gp + 128));
       }
+
       // chunk loop: this warp serves query row rr of the unit (TMEM lanes 16 rr .. 16 rr + 15);
       // thread t holds heads hA = t/4 and hB = hA + 8, keys kq, kq + 1 of every block
       const uint32_t* rb_row = rb + rr * (K4U_MAXU / 32);
-      const int64_t ir = (u % ntiles) * 8 + rr;
+      const int64_t ir = (uid % ntiles) * 8 + rr;
       const int32_t own_r = meta[1 + rr];
       const int32_t tlim_r = (int32_t)((a.pos0 + ir) & 7);
       float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
@@ -600,14 +610,12 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         lb += __shfl_xor_sync(0xffffffffu, lb, o);
       }
       float* xl = xchg;
+      float* xm = xchg + 128;
       if ((lane & 3) == 0) {
         xl[16 * rr + hA] = la;
         xl[16 * rr + hB] = lb;
-        if (ir < a.rows && a.lse) {
-          const int64_t hr = ir * a.H + (int64_t)g * 16;
-          a.lse[hr + hA] = (ma + __log2f(la)) * 0.6931471805599453f;
-          a.lse[hr + hB] = (mb + __log2f(lb)) * 0.6931471805599453f;
-        }
+        xm[16 * rr + hA] = ma;
+        xm[16 * rr + hB] = mb;
       }
       kc += (uint32_t)nch;
       // the next unit's Q goes in now: its first S overlaps this epilogue
@@ -621,7 +629,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       float gh = 0.f;
       if (row_ok && !a.gate_per_dim) gh = __bfloat162float(a.gate[hb]);
       if (sync_stop()) break;
-      const float lt = xl[m];
+      const float lt = xl[m], mt = xm[m];
+      if (hf == 0 && row_ok && a.lse) a.lse[hb] = (mt + __log2f(lt)) * 0.6931471805599453f;
       if (!wait_ok(kPvDone, (kc - 1) & 1)) continue;  // caught at the next unit's barrier
       tc_fence_after();
       const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
@@ -674,5 +683,6 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
+
 
 }  // namespace sgqa

@@ -22,6 +22,7 @@
 #include "k3_topk.cuh"
 #include "k4_attention.cuh"
 #include "k4u_attention.cuh"
+#include "k4r_route.cuh"
 
 using namespace sgqa;
 
@@ -59,7 +60,8 @@ sgqa_status check_params(const sgqa_params* p, Prm& o) {
   const int B = p->block_size;
   if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED_SHAPE;
   if (p->gate_per_dim != 0 && p->gate_per_dim != 1) return SGQA_ERR_INVALID_ARGUMENT;
-  if (p->attn_kernel != SGQA_ATTN_AUTO && p->attn_kernel != SGQA_ATTN_WARP && p->attn_kernel != SGQA_ATTN_TC_UNION)
+  if (p->attn_kernel != SGQA_ATTN_AUTO && p->attn_kernel != SGQA_ATTN_WARP && p->attn_kernel != SGQA_ATTN_TC_UNION &&
+      p->attn_kernel != SGQA_ATTN_ROUTED)
     return SGQA_ERR_INVALID_ARGUMENT;
   o.G = p->num_kv_groups;
   o.Hg = p->heads_per_group;
@@ -213,15 +215,35 @@ IndexWs index_ws_layout(const Prm& p, int64_t rows, int64_t max_cand) {
 // One CTA per row; the block is the smallest whose registers (32 keys per thread) hold
 // the launch's longest row, so short rows do not pay for empty slots.  Longer rows go
 // through the segment + merge pair when `wsl` gives them pair buffers inside `ws`.
+// Register-resident top-k launch for rows of at most NT * PER candidates, PER the
+// smallest multiple of 4 that holds max_cand (at least 8): short rows do not pay for
+// empty slots.
+template <int NT>
+void launch_k3_regs(const K3Args& a, int64_t max_cand, int64_t grid, cudaStream_t st) {
+  const int per = (int)std::max<int64_t>(8, cdiv(cdiv(max_cand, NT), 4) * 4);
+  switch (per) {
+    case 8: k3_topk<NT, 8, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 12: k3_topk<NT, 12, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 16: k3_topk<NT, 16, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 20: k3_topk<NT, 20, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 24: k3_topk<NT, 24, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 28: k3_topk<NT, 28, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    default: k3_topk<NT, 32, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+  }
+}
+
+// One CTA per row; the block is the smallest whose registers (up to 32 keys per thread)
+// hold the launch's longest row.  Longer rows go through the segment + merge pair when
+// `wsl` gives them pair buffers inside `ws`.
 cudaError_t launch_k3(K3Args a, int64_t max_cand, uint8_t* ws, const IndexWs& wsl, cudaStream_t st) {
   const int64_t grid = (int64_t)a.G * a.rows;
   if (grid <= 0) return cudaSuccess;
   if (max_cand <= 128 * kK3Per) {
-    k3_topk<128, kK3Per, false><<<(unsigned)grid, 128, 0, st>>>(a);
+    launch_k3_regs<128>(a, max_cand, grid, st);
   } else if (max_cand <= 256 * kK3Per) {
-    k3_topk<256, kK3Per, false><<<(unsigned)grid, 256, 0, st>>>(a);
+    launch_k3_regs<256>(a, max_cand, grid, st);
   } else if (max_cand <= kK3RegRow) {
-    k3_topk<kK3Threads, kK3Per, false><<<(unsigned)grid, kK3Threads, 0, st>>>(a);
+    launch_k3_regs<kK3Threads>(a, max_cand, grid, st);
   } else if (wsl.nseg > 0 && cdiv(max_cand, kK3RegRow) <= wsl.nseg) {
     a.nseg = (int32_t)cdiv(max_cand, kK3RegRow);
     a.pair_key = reinterpret_cast<uint32_t*>(ws + wsl.pair_key);
@@ -335,16 +357,34 @@ bool union_fits(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
          (q_start + T - 1) / 8 < (int64_t)K4U_MAX_BLOCKS;
 }
 
-// The attention kernel a call launches (SGQA_ATTN_WARP or SGQA_ATTN_TC_UNION), following
+// The attention kernel a call launches (SGQA_ATTN_WARP, _TC_UNION or _ROUTED), following
 // sgqa_params.attn_kernel; -1 when the requested kernel cannot serve these arguments.
-int attn_choice(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
+// ws_ok: the call's workspace holds the routed mode's buffers (attn_ws_layout).
+int attn_choice(const Prm& p, int32_t dense, int64_t T, int64_t q_start, bool ws_ok) {
   const bool fits = union_fits(p, dense, T, q_start);
   switch (p.attn_kernel) {
-    case SGQA_ATTN_AUTO: return fits ? SGQA_ATTN_TC_UNION : SGQA_ATTN_WARP;
+    case SGQA_ATTN_AUTO: return fits ? (ws_ok ? SGQA_ATTN_ROUTED : SGQA_ATTN_TC_UNION) : SGQA_ATTN_WARP;
     case SGQA_ATTN_WARP: return SGQA_ATTN_WARP;
     case SGQA_ATTN_TC_UNION: return fits ? SGQA_ATTN_TC_UNION : -1;
+    case SGQA_ATTN_ROUTED: return fits ? SGQA_ATTN_ROUTED : -1;
   }
   return -1;
+}
+
+// Workspace of the routed attention mode for T query rows: the per-unit choice, the two
+// unit lists and their lengths (units = G x ceil(T / 8)).
+struct AttnWs {
+  size_t choice, union_units, warp_units, counts, total;
+};
+AttnWs attn_ws_layout(const Prm& p, int64_t T) {
+  AttnWs w{};
+  const size_t nu = (size_t)p.G * (size_t)cdiv(std::max<int64_t>(T, 0), 8);
+  w.choice = 0;
+  w.union_units = align_up(nu * 4, 256);
+  w.warp_units = w.union_units + align_up(nu * 4, 256);
+  w.counts = w.warp_units + align_up(nu * 4, 256);
+  w.total = w.counts + 256;
+  return w;
 }
 
 cudaError_t launch_k4u(const K4UArgs& a, const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
@@ -359,10 +399,66 @@ cudaError_t launch_k4u(const K4UArgs& a, const CUtensorMap& tk, const CUtensorMa
 
 sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void* v, int64_t ctx_cap, const void* gate,
                           const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T, int64_t q_start, void* out,
-                          float* lse, int32_t dense, cudaStream_t st) {
-  const int kernel = attn_choice(p, dense, T, q_start);
+                          float* lse, int32_t dense, void* ws, size_t ws_bytes, cudaStream_t st) {
+  const AttnWs wl = attn_ws_layout(p, T);
+  const bool ws_ok = ws && aligned16(ws) && ws_bytes >= wl.total;
+  const int kernel = attn_choice(p, dense, T, q_start, ws_ok);
   if (kernel < 0) return SGQA_ERR_UNSUPPORTED_SHAPE;
-  if (kernel == SGQA_ATTN_TC_UNION) {
+  if (kernel == SGQA_ATTN_ROUTED && !ws_ok) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  const uint64_t kv_rows = (uint64_t)p.G * ctx_cap;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const int32_t* union_units = nullptr;
+  const int32_t* counts = nullptr;
+  if (kernel == SGQA_ATTN_ROUTED) {
+    // each 8-row unit to the kernel that serves it more cheaply (k4r_route.cuh): the
+    // warp-level kernel takes its list here, the union kernel below takes the other
+    K4RouteArgs ra{};
+    ra.sel_idx = sel_idx;
+    ra.sel_cnt = sel_cnt;
+    ra.choice = reinterpret_cast<int32_t*>(w + wl.choice);
+    ra.union_units = reinterpret_cast<int32_t*>(w + wl.union_units);
+    ra.warp_units = reinterpret_cast<int32_t*>(w + wl.warp_units);
+    ra.counts = reinterpret_cast<int32_t*>(w + wl.counts);
+    ra.rows = T;
+    ra.pos0 = q_start;
+    ra.G = p.G;
+    ra.kcap = p.k;
+    const int64_t n_units = (int64_t)p.G * cdiv(T, 8);
+    k4r_count<<<(unsigned)cdiv(n_units, K4R_WARPS), K4R_WARPS * 32, 0, st>>>(ra);
+    SGQA_CUDA_OK(cudaGetLastError());
+    k4r_compact<<<1, K4R_COMPACT_THREADS, 0, st>>>(ra);
+    SGQA_CUDA_OK(cudaGetLastError());
+    union_units = ra.union_units;
+    counts = ra.counts;
+    K4Args a{};
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.gate = static_cast<const __nv_bfloat16*>(gate);
+    a.kc = static_cast<const __nv_bfloat16*>(k);
+    a.vc = static_cast<const __nv_bfloat16*>(v);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.lse = lse;
+    a.sel_idx = sel_idx;
+    a.sel_cnt = sel_cnt;
+    a.rows = T;
+    a.pos0 = q_start;
+    a.ctx_cap = ctx_cap;
+    a.G = p.G;
+    a.Hg = p.Hg;
+    a.H = p.H;
+    a.B = p.B;
+    a.kcap = p.k;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.gate_per_dim = p.gate_per_dim;
+    a.nsplit = 1;
+    a.units = ra.warp_units;
+    a.n_units_dev = ra.counts + 1;
+    a.wait_ns = g_wait_ns;
+    CUtensorMap tk, tv;
+    if (!make_kv_map(&tk, k, kv_rows) || !make_kv_map(&tv, v, kv_rows)) return SGQA_ERR_CUDA;
+    // one CTA of 8 warps per listed unit; CTAs past the list's length return at once
+    SGQA_CUDA_OK(launch_k4(a, tk, tv, n_units * 8, true, st));
+  }
+  if (kernel == SGQA_ATTN_TC_UNION || kernel == SGQA_ATTN_ROUTED) {
     K4UArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.gate = static_cast<const __nv_bfloat16*>(gate);
@@ -379,9 +475,10 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
     a.scale_log2 = p.scale * 1.4426950408889634f;
     a.gate_per_dim = p.gate_per_dim;
     a.wait_ns = g_wait_ns;
+    a.units = union_units;
+    a.n_units_dev = counts;
     CUtensorMap tk, tv;
-    const uint64_t rowsz = (uint64_t)p.G * ctx_cap;
-    if (!make_kv_map(&tk, k, rowsz) || !make_kv_map(&tv, v, rowsz)) return SGQA_ERR_CUDA;
+    if (!make_kv_map(&tk, k, kv_rows) || !make_kv_map(&tv, v, kv_rows)) return SGQA_ERR_CUDA;
     SGQA_CUDA_OK(launch_k4u(a, tk, tv, st));
     return SGQA_OK;
   }
@@ -416,6 +513,13 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
   }
   SGQA_CUDA_OK(launch_k4(a, tk, tv, (int64_t)p.G * T, tma, st));
   return SGQA_OK;
+}
+
+// Workspace the attention entries want for T rows ending at ctx_len: the routed mode's when
+// the union kernel can serve the call (positions q_start = ctx_len - T onwards), else none.
+size_t attn_ws_bytes(const Prm& p, int64_t T, int64_t ctx_len) {
+  if (T <= 0 || !union_fits(p, 0, T, std::max<int64_t>(0, ctx_len - T))) return 0;
+  return attn_ws_layout(p, T).total;
 }
 
 // ---- scratch for the allocation-free indexer entry ----
@@ -466,7 +570,8 @@ HostWs host_ws_layout(const Prm& p, int64_t R, int64_t ctx_len) {
   w.sel = 2 * qp;
   w.cnt = w.sel + align_up((size_t)p.G * R * p.k * 4, 256);
   w.index = w.cnt + align_up((size_t)p.G * R * 4, 256);
-  w.index_bytes = std::max<size_t>(256, index_ws_bytes(p, R, (ctx_len - 1) / p.B));
+  // one chunk's indexer + top-k scratch, reused by its attention (the routed mode's lists)
+  w.index_bytes = std::max<size_t>({256, index_ws_bytes(p, R, (ctx_len - 1) / p.B), attn_ws_bytes(p, R, ctx_len)});
   w.total = w.index + w.index_bytes;
   return w;
 }
@@ -535,7 +640,7 @@ int32_t sgqa_abi_version(void) { return SGQA_ABI_VERSION; }
 int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode) {
   Prm p;
   if (check_params(prm, p) != SGQA_OK || T < 0 || q_start < 0) return -1;
-  return attn_choice(p, dense_mode ? 1 : 0, T, q_start);
+  return attn_choice(p, dense_mode ? 1 : 0, T, q_start, true);
 }
 
 sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns) {
@@ -564,10 +669,13 @@ size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64
   const int64_t max_cand = (ctx_len - 1) / p.B;
   switch (op) {
     case SGQA_OP_INDEX_TOPK:
-    case SGQA_OP_PREFILL:
       return std::max<size_t>(256, index_ws_bytes(p, std::min<int64_t>(std::max<int64_t>(T, 1), kIndexChunkRows), max_cand));
+    case SGQA_OP_PREFILL:  // the stages run one after another: they share the workspace
+      return std::max<size_t>(
+          {256, index_ws_bytes(p, std::min<int64_t>(std::max<int64_t>(T, 1), kIndexChunkRows), max_cand),
+           attn_ws_bytes(p, T, ctx_len)});
     case SGQA_OP_ATTN:
-      return 256;
+      return std::max<size_t>(256, attn_ws_bytes(p, T, ctx_len));
     case SGQA_OP_PREFILL_HOST:
       return host_ws_layout(p, host_chunk_rows(p, T, batch), ctx_len).total;
     case SGQA_OP_DECODE: {
@@ -658,7 +766,8 @@ sgqa_status sgqa_index_topk_noalloc(const sgqa_params* prm, const void* q_proxy,
 
 sgqa_status sgqa_sparse_attn_fwd(const sgqa_params* prm, const void* q, const void* k, const void* v, int64_t ctx_cap,
                                  const void* gate, const int32_t* sel_idx, const int32_t* sel_cnt, int64_t T,
-                                 int64_t q_start, void* out, float* lse, int32_t dense_mode, sgqa_stream_t stream) {
+                                 int64_t q_start, void* out, float* lse, int32_t dense_mode, void* ws, size_t ws_bytes,
+                                 sgqa_stream_t stream) {
   Prm p;
   sgqa_status s = check_params(prm, p);
   if (s != SGQA_OK) return s;
@@ -669,8 +778,8 @@ sgqa_status sgqa_sparse_attn_fwd(const sgqa_params* prm, const void* q, const vo
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (p.gate_per_dim && !aligned16(gate)))
     return SGQA_ERR_INVALID_ARGUMENT;
   if (T == 0) return SGQA_OK;
-  return run_attention(p, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, dense_mode ? 1 : 0,
-                       reinterpret_cast<cudaStream_t>(stream));
+  return run_attention(p, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, dense_mode ? 1 : 0, ws,
+                       ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, const void* v, const void* gate,
@@ -687,11 +796,18 @@ sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, c
   if (cdiv(q_start + T, p.B) > nb_cap) return SGQA_ERR_INVALID_ARGUMENT;
   if ((int64_t)p.G * ctx_cap > (int64_t)INT32_MAX) return SGQA_ERR_UNSUPPORTED_SHAPE;
   if (!ws) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  // the attention stage's own checks, made before anything is enqueued
+  const bool attn_ws_ok = aligned16(ws) && ws_bytes >= attn_ws_layout(p, T).total;
+  const int kernel = attn_choice(p, 0, T, q_start, attn_ws_ok);
+  if (kernel < 0) return SGQA_ERR_UNSUPPORTED_SHAPE;
+  if (kernel == SGQA_ATTN_ROUTED && !attn_ws_ok) return SGQA_ERR_WORKSPACE_TOO_SMALL;
   s = sgqa_build_block_index(prm, k_proxy, ctx_cap, q_start, q_start + T, k_blk, nb_cap, stream);
   if (s != SGQA_OK) return s;
   s = sgqa_index_topk(prm, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, ws_bytes, stream);
   if (s != SGQA_OK) return s;
-  return sgqa_sparse_attn_fwd(prm, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, 0, stream);
+  // the indexer's scratch is dead once the top-k has run: the attention reuses the workspace
+  return sgqa_sparse_attn_fwd(prm, q, k, v, ctx_cap, gate, sel_idx, sel_cnt, T, q_start, out, lse, 0, ws, ws_bytes,
+                              stream);
 }
 
 sgqa_status sgqa_prefill_host(const sgqa_params* prm, const sgqa_host_tensors* host, const sgqa_device_tensors* dev,
@@ -714,7 +830,8 @@ sgqa_status sgqa_prefill_host(const sgqa_params* prm, const sgqa_host_tensors* h
   if (!d.ws || d.ws_bytes < wl.total) return SGQA_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(d.ws)) return SGQA_ERR_INVALID_ARGUMENT;
   // the same checks sgqa_prefill makes on every chunk, made once before anything is enqueued
-  if (attn_choice(p, 0, std::min(T, R), q_start) < 0 || attn_choice(p, 0, T - (T - 1) / R * R, q_start + (T - 1) / R * R) < 0)
+  if (attn_choice(p, 0, std::min(T, R), q_start, true) < 0 ||
+      attn_choice(p, 0, T - (T - 1) / R * R, q_start + (T - 1) / R * R, true) < 0)
     return SGQA_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(d.q) || !aligned16(d.k) || !aligned16(d.v) || !aligned16(d.out) || !aligned16(d.k_proxy) ||
       !aligned16(d.k_blk) || (p.gate_per_dim && !aligned16(d.gate)))
@@ -933,7 +1050,7 @@ static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64
     c.H = p.H;
     c.nsplit = nsplit;
     c.gate_per_dim = p.gate_per_dim;
-    const int64_t warps = (int64_t)p.G * batch * p.Hg;
+    const int64_t warps = (int64_t)p.G * batch * p.Hg * K4C_SLICES;
     k4_combine<<<(unsigned)cdiv(warps * 32, 128), 128, 0, st>>>(c);  // 4 warps per CTA: spread over the SMs
     SGQA_CUDA_OK(cudaGetLastError());
   }

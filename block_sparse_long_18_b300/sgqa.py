@@ -46,7 +46,7 @@ EXPORTS = (
     "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc", "sgqa_attention_kernel",
     "sgqa_build_block_index_fp8", "sgqa_decode_fp8", "sgqa_prefill_host",
 )
-ATTN_AUTO, ATTN_WARP, ATTN_TC_UNION = 0, 1, 2
+ATTN_AUTO, ATTN_WARP, ATTN_TC_UNION, ATTN_ROUTED = 0, 1, 2, 3
 
 
 class SgqaError(RuntimeError):
@@ -72,7 +72,8 @@ class Params(ctypes.Structure):
 def params(G=4, Hg=16, D=192, P=256, B=8, k=512, gate_per_dim=1, scale=0.0, attn_kernel=ATTN_AUTO) -> Params:
     """Layer constants; the defaults are the pages' (phantomic12 entry: 64 heads in 4 KV
     groups, head_dim 192, topk 512, proxy_dim 256; ai4snews item: block size 8).
-    attn_kernel: ATTN_AUTO, or ATTN_WARP / ATTN_TC_UNION to force a prefill attention kernel."""
+    attn_kernel: ATTN_AUTO, or ATTN_WARP / ATTN_TC_UNION / ATTN_ROUTED to force a prefill
+    attention kernel."""
     return Params(G, Hg, D, P, B, k, gate_per_dim, scale, attn_kernel)
 
 
@@ -101,7 +102,8 @@ _lib.sgqa_attention_kernel.argtypes = [_PP, _I64, _I64, ctypes.c_int32]
 _lib.sgqa_build_block_index.argtypes = [_PP, _P, _I64, _I64, _I64, _P, _I64, _P]
 _lib.sgqa_index_topk.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P, ctypes.c_size_t, _P]
 _lib.sgqa_index_topk_noalloc.argtypes = [_PP, _P, _I64, _I64, _P, _I64, _P, _P, _P]
-_lib.sgqa_sparse_attn_fwd.argtypes = [_PP, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, ctypes.c_int32, _P]
+_lib.sgqa_sparse_attn_fwd.argtypes = [_PP, _P, _P, _P, _I64, _P, _P, _P, _I64, _I64, _P, _P, ctypes.c_int32, _P,
+                                      ctypes.c_size_t, _P]
 _lib.sgqa_prefill.argtypes = [_PP, _P, _P, _P, _P, _P, _P, _I64, _I64, _I64, _P, _I64, _P, _P, _P, _P, _P,
                               ctypes.c_size_t, _P]
 _lib.sgqa_decode.argtypes = [_PP, ctypes.c_int32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _P, _P, _P, _P,
@@ -203,12 +205,15 @@ def sgqa_index_topk_noalloc(prm: Params, q_proxy, q_start: int, k_blk, sel_idx, 
 
 
 def sgqa_sparse_attn_fwd(prm: Params, q, k, v, gate, sel_idx, sel_cnt, q_start: int, out, lse=None,
-                         dense_mode: bool = False, stream=None):
+                         dense_mode: bool = False, stream=None, ws=None):
+    """ws: optional uint8 workspace of sgqa_workspace_bytes(prm, SGQA_OP_ATTN, T, q_start + T)
+    bytes; it enables the routed mode (the default where the union kernel's shape holds)."""
     T = q.shape[0]
     _check(_lib.sgqa_sparse_attn_fwd(ctypes.byref(prm), _dev(q, BF16, "q"), _dev(k, BF16, "k"), _dev(v, BF16, "v"),
                                      k.shape[1], _dev(gate, BF16, "gate"), _dev(sel_idx, I32, "sel_idx"),
                                      _dev(sel_cnt, I32, "sel_cnt"), T, q_start, _dev(out, BF16, "out"),
-                                     _dev(lse, F32, "lse"), 1 if dense_mode else 0, _stream(stream)),
+                                     _dev(lse, F32, "lse"), 1 if dense_mode else 0,
+                                     _dev(ws, torch.uint8, "ws"), 0 if ws is None else ws.numel(), _stream(stream)),
            "sgqa_sparse_attn_fwd")
 
 

@@ -71,7 +71,7 @@ typedef struct {
   int32_t gate_per_dim;     /* 1: gate is [T, H, D] (element-wise); 0: gate is [T, H] (per head) */
   float softmax_scale;      /* scale on q.k; <= 0 selects 1/sqrt(D) */
   int32_t attn_kernel;      /* prefill attention kernel: SGQA_ATTN_AUTO (0, the default), or
-                               SGQA_ATTN_WARP / SGQA_ATTN_TC_UNION to force one (see
+                               SGQA_ATTN_WARP / _TC_UNION / _ROUTED to force one (see
                                sgqa_attention_kernel); other values are INVALID_ARGUMENT */
 } sgqa_params;
 
@@ -80,6 +80,9 @@ typedef struct {
 #define SGQA_ATTN_WARP 1      /* one warp per (row, group) on warp-level MMAs: every shape */
 #define SGQA_ATTN_TC_UNION 2  /* 8 query rows per unit over the union of their selected blocks,
                                  tcgen05 with the (row, head) pairs as the MMA's M */
+#define SGQA_ATTN_ROUTED 3    /* each unit of 8 query rows to the union kernel when its union is
+                                 small against its rows' selections (they share many blocks),
+                                 else to the warp-level kernel (needs the attention workspace) */
 
 /* Operation selector for sgqa_workspace_bytes(). */
 enum { SGQA_OP_INDEX_TOPK = 1, SGQA_OP_PREFILL = 2, SGQA_OP_DECODE = 3, SGQA_OP_ATTN = 4, SGQA_OP_PREFILL_HOST = 5 };
@@ -143,13 +146,19 @@ SGQA_API sgqa_status sgqa_index_topk(const sgqa_params* prm, const void* q_proxy
  *   k, v     [G, ctx_cap, D] bf16, read (group-major: a block of a group is contiguous)
  *   sel_idx  [G, T, k] int32 ascending, sel_cnt [G, T] int32, read (ignored in dense_mode)
  *   out      [T, H, D] bf16, written;  lse [T, H] fp32, written (may be NULL)
+ *   ws       scratch of sgqa_workspace_bytes(prm, SGQA_OP_ATTN, T, q_start + T, 1) bytes
+ *            (G * ceil(T/8) * 12 bytes + 256, under 1 MB at T = 131,072), 16-byte aligned, or
+ *            NULL / too small: the routed mode (SGQA_ATTN_ROUTED, the default where the union
+ *            kernel's shape holds) keeps its per-unit choice and unit lists there; without
+ *            it every unit runs on the union kernel.
  * A sel_idx entry outside [0, b_t] sets SGQA_ERR_DEVICE_BOUNDS on the device and the
- * entry is skipped.  Errors: INVALID_ARGUMENT, UNSUPPORTED_SHAPE.
+ * entry is skipped.  Errors: INVALID_ARGUMENT, UNSUPPORTED_SHAPE (a forced kernel outside
+ * its shape), WORKSPACE_TOO_SMALL (SGQA_ATTN_ROUTED forced without the workspace).
  * ------------------------------------------------------------------------------- */
 SGQA_API sgqa_status sgqa_sparse_attn_fwd(const sgqa_params* prm, const void* q, const void* k, const void* v,
                                  int64_t ctx_cap, const void* gate, const int32_t* sel_idx,
                                  const int32_t* sel_cnt, int64_t T, int64_t q_start, void* out, float* lse,
-                                 int32_t dense_mode, sgqa_stream_t stream);
+                                 int32_t dense_mode, void* ws, size_t ws_bytes, sgqa_stream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * Fused prefill of one Sparse GQA layer: block index over [q_start, q_start+T), then
@@ -160,7 +169,8 @@ SGQA_API sgqa_status sgqa_sparse_attn_fwd(const sgqa_params* prm, const void* q,
  *   q, gate [T, H, D]; q_proxy [G, T, P]; k, v [G, ctx_cap, D]; k_proxy [G, ctx_cap, P]
  *   k_blk   [G, nb_cap, P] (read and written); sel_idx [G, T, k]; sel_cnt [G, T]
  *   out [T, H, D] bf16; lse [T, H] fp32 or NULL
- *   ws      >= sgqa_workspace_bytes(prm, SGQA_OP_PREFILL, T, q_start + T, 1)
+ *   ws      >= sgqa_workspace_bytes(prm, SGQA_OP_PREFILL, T, q_start + T, 1): the indexer +
+ *           top-k scratch, then (reused) the attention's (see sgqa_sparse_attn_fwd)
  * ------------------------------------------------------------------------------- */
 SGQA_API sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, const void* v,
                          const void* gate, const void* q_proxy, const void* k_proxy, int64_t ctx_cap,
@@ -322,13 +332,15 @@ SGQA_API sgqa_status sgqa_set_wait_timeout_ns(uint64_t ns);
 SGQA_API sgqa_status sgqa_selftest_wait_timeout(uint64_t limit_ns, sgqa_stream_t stream);
 
 /* Which attention kernel sgqa_sparse_attn_fwd / sgqa_prefill launch for these arguments
- * (no launch, no device access).  With prm->attn_kernel = SGQA_ATTN_AUTO: SGQA_ATTN_TC_UNION
- * whenever its shape holds (blocks of 8, 16 heads per group, top_k_blocks <= 512, every
- * block index of the call below 2^17, i.e. positions below 1,048,576, not dense_mode),
- * SGQA_ATTN_WARP otherwise.  A forced kernel is returned when it can serve the call; a
- * forced SGQA_ATTN_TC_UNION outside its shape returns -1, and the attention entries then
- * fail with SGQA_ERR_UNSUPPORTED_SHAPE.  Returns -1 for invalid parameters.  Decode always
- * runs the warp-level kernel (split over the context). */
+ * given a workspace of sgqa_workspace_bytes(...) bytes (no launch, no device access).  With
+ * prm->attn_kernel = SGQA_ATTN_AUTO: SGQA_ATTN_ROUTED whenever the union kernel's shape
+ * holds (blocks of 8, 16 heads per group, top_k_blocks <= 512, every block index of the
+ * call below 2^18, i.e. positions below 2,097,152, not dense_mode), SGQA_ATTN_WARP
+ * otherwise (an attention call without the workspace runs SGQA_ATTN_TC_UNION instead of
+ * the routed mode).  A forced kernel is returned when it can serve the call; a forced union
+ * or routed kernel outside its shape returns -1, and the attention entries then fail with
+ * SGQA_ERR_UNSUPPORTED_SHAPE.  Returns -1 for invalid parameters.  Decode always runs the
+ * warp-level kernel (split over the context). */
 SGQA_API int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode);
 
 /* Short English description of a status code (static storage). */

@@ -100,21 +100,25 @@ def test_decode_validation(lib):
 def test_workspace_sizes(lib):
     prm = lib.params()
     # 128K prefill: one pass of 8,192 rows x 4 groups x 16,384 fp32 candidates
-    ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL, 131072, 131072)
+    ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 131072, 131072)
     assert ws == 4 * 8192 * 16384 * 4
+    # prefill: the indexer's scratch, reused by the routed attention's unit lists
+    wa = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_ATTN, 131072, 131072)
+    assert wa < (1 << 20) and lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL, 131072, 131072) == ws
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 8) > 0
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 0) == 0
     assert lib.sgqa_workspace_bytes(lib.params(B=3), lib.SGQA_OP_PREFILL, 16, 16) == 0
 
 
 def test_attention_kernel_choice(lib):
-    """Which prefill attention kernel a call launches (no device access): the union kernel
-    wherever its shape holds, up to the 1M-token context; the warp-level kernel for other
-    shapes, dense mode and when forced; -1 for a forced union outside its shape."""
+    """Which prefill attention kernel a call launches (no device access): the routed mode
+    (union or warp-level kernel per 8-row unit) wherever the union kernel's shape holds, up
+    to 2M positions; the warp-level kernel for other shapes, dense mode and when forced; -1
+    for a forced union outside its shape."""
     auto = lib.params()
-    assert lib.sgqa_attention_kernel(auto, 131072, 0) == lib.ATTN_TC_UNION
-    assert lib.sgqa_attention_kernel(auto, 8192, 1040384) == lib.ATTN_TC_UNION   # the 1M chunk
-    assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8192) == lib.ATTN_TC_UNION
+    assert lib.sgqa_attention_kernel(auto, 131072, 0) == lib.ATTN_ROUTED
+    assert lib.sgqa_attention_kernel(auto, 8192, 1040384) == lib.ATTN_ROUTED   # the 1M chunk
+    assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8192) == lib.ATTN_ROUTED
     assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8191) == lib.ATTN_WARP  # past 2^18 blocks
     assert lib.sgqa_attention_kernel(auto, 1024, 0, dense_mode=True) == lib.ATTN_WARP
     assert lib.sgqa_attention_kernel(lib.params(B=4, k=1024), 1024, 0) == lib.ATTN_WARP
@@ -126,6 +130,9 @@ def test_attention_kernel_choice(lib):
     assert lib.sgqa_attention_kernel(union, 131072, 0) == lib.ATTN_TC_UNION
     assert lib.sgqa_attention_kernel(lib.params(B=16, k=256, attn_kernel=lib.ATTN_TC_UNION), 1024, 0) == -1
     assert lib.sgqa_attention_kernel(union, 1024, 0, dense_mode=True) == -1
+    routed = lib.params(attn_kernel=lib.ATTN_ROUTED)
+    assert lib.sgqa_attention_kernel(routed, 131072, 0) == lib.ATTN_ROUTED
+    assert lib.sgqa_attention_kernel(lib.params(B=4, k=1024, attn_kernel=lib.ATTN_ROUTED), 1024, 0) == -1
     assert lib.sgqa_attention_kernel(lib.params(attn_kernel=7), 1024, 0) == -1
 
 
@@ -133,8 +140,15 @@ def test_forced_union_outside_its_shape_is_rejected(lib):
     prm = lib.params(B=16, k=256, attn_kernel=lib.ATTN_TC_UNION)
     a = ctypes.c_void_p(1 << 12)
     f = lib._lib.sgqa_sparse_attn_fwd
-    assert f(ctypes.byref(prm), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None) == 2
-    assert f(ctypes.byref(lib.params(attn_kernel=3)), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None) == 1
+    assert f(ctypes.byref(prm), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None, 0, None) == 2
+    assert f(ctypes.byref(lib.params(attn_kernel=9)), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None, 0, None) == 1
+    # the routed mode forced without its workspace (a choice and two lists per 8-row unit)
+    routed = lib.params(attn_kernel=lib.ATTN_ROUTED)
+    need = lib.sgqa_workspace_bytes(routed, lib.SGQA_OP_ATTN, 1024, 4096)
+    assert need >= 4 * 128 * 12 + 256
+    assert f(ctypes.byref(routed), a, a, a, 4096, a, a, a, 1024, 3072, a, None, 0, a, need - 256, None) == 3
+    # no workspace needed where the union kernel cannot serve
+    assert lib.sgqa_workspace_bytes(lib.params(B=4, k=1024), lib.SGQA_OP_ATTN, 1024, 4096) == 256
 
 
 def test_prefill_host_validation(lib):

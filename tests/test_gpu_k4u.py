@@ -1,8 +1,10 @@
 """Parity of the union attention kernel (8 query rows per unit over the union of their
-selected blocks, tcgen05 with Q and P in tensor memory) against the oracle, and of the
-warp-level kernel it replaces.  Each is forced through sgqa_params.attn_kernel, and every
-case first asserts through sgqa_attention_kernel that the forced kernel is the one the
-call launches."""
+selected blocks, tcgen05 with Q and P in tensor memory), of the warp-level kernel, and of
+the routed mode (each 8-row unit to one of the two by the size of its union) against the
+oracle.  Each is forced through sgqa_params.attn_kernel, and every case first asserts
+through sgqa_attention_kernel that the forced kernel is the one the call launches.  The
+routed mode is also checked bit for bit: every unit's output is the union kernel's or the
+warp-level kernel's, whichever a host restatement of the routing rule picks."""
 import numpy as np
 import pytest
 import torch
@@ -75,15 +77,73 @@ def test_union_attention_sampled_rows_long_context(sg, case):
     _run_case(sg, sg.ATTN_TC_UNION, case)
 
 
+@pytest.mark.parametrize("case", UNION_CASES, ids=[f"T{c['T']}_k{c['k']}_q{c.get('q_start', 0)}" for c in UNION_CASES])
+def test_routed_attention_all_rows(sg, case):
+    _run_case(sg, sg.ATTN_ROUTED, case)
+
+
+@pytest.mark.parametrize("case", UNION_SAMPLED, ids=[f"q{c['q_start']}_T{c['T']}" for c in UNION_SAMPLED])
+def test_routed_attention_sampled_rows_long_context(sg, case):
+    _run_case(sg, sg.ATTN_ROUTED, case)
+
+
+def _route_to_union(sel_idx, sel_cnt, q_start, k):
+    """Host restatement of the routing rule: per (group, 8-row unit), the distinct valid
+    blocks of its rows' selections (counts clamped to [1, min(k, b_t + 1)], entries outside
+    [0, b_t] ignored) against its (row, block) pairs; union iff
+    100 * windows * |union| <= 55 * pairs, windows = 16,384-block windows its own blocks reach."""
+    G, T, _ = sel_idx.shape
+    out = np.zeros((G, (T + 7) // 8), dtype=bool)
+    for g in range(G):
+        for u in range((T + 7) // 8):
+            blocks, pairs = set(), 0
+            windows = ((q_start + min(T, u * 8 + 8) - 1) // 8) // 16384 + 1
+            for i in range(u * 8, min(T, u * 8 + 8)):
+                bt = (q_start + i) // 8
+                c = int(sel_cnt[g, i])
+                c = 1 if c < 1 else min(c, min(k, bt + 1))
+                pairs += c
+                blocks.update(int(b) for b in sel_idx[g, i, :c] if 0 <= b <= bt)
+            out[g, u] = 100 * windows * len(blocks) <= 55 * pairs
+    return out
+
+
+@pytest.mark.parametrize("case", [dict(T=1024, G=2, Hg=16, B=8, k=512, q_start=60000, planted=True),
+                                  dict(T=2000, G=1, Hg=16, B=8, k=128, q_start=20003, planted=True)],
+                         ids=["q60000_k512", "q20003_k128"])
+def test_routed_units_match_the_chosen_kernel_bit_for_bit(sg, case):
+    """Routed mode: each unit's outputs and LSE are exactly those of the kernel the rule
+    picks for it (both kernels are deterministic), and the call uses both kernels."""
+    wl = gen.small_workload(**case)
+    inp = _to_cuda(gen.make_inputs(wl, seed=29))
+    res = {}
+    for kern in (sg.ATTN_TC_UNION, sg.ATTN_WARP, sg.ATTN_ROUTED):
+        prm = _prm(sg, wl)
+        prm.attn_kernel = kern
+        res[kern] = _gpu_prefill(sg, inp, wl, prm)
+    assert torch.equal(res[sg.ATTN_ROUTED].sel_idx, res[sg.ATTN_TC_UNION].sel_idx)
+    to_union = _route_to_union(res[sg.ATTN_ROUTED].sel_idx.cpu().numpy(), res[sg.ATTN_ROUTED].sel_cnt.cpu().numpy(),
+                               wl.q_start, wl.k)
+    assert to_union.any() and (~to_union).any(), "the case should use both kernels"
+    out = {kk: r.out.view(wl.T, wl.G, wl.Hg, wl.D) for kk, r in res.items()}
+    lse = {kk: r.lse.view(wl.T, wl.G, wl.Hg) for kk, r in res.items()}
+    for g in range(wl.G):
+        for u in range(to_union.shape[1]):
+            src = sg.ATTN_TC_UNION if to_union[g, u] else sg.ATTN_WARP
+            rows = slice(u * 8, min(wl.T, u * 8 + 8))
+            assert torch.equal(out[sg.ATTN_ROUTED][rows, g], out[src][rows, g]), (g, u, src)
+            assert torch.equal(lse[sg.ATTN_ROUTED][rows, g], lse[src][rows, g]), (g, u, src)
+
+
 @pytest.mark.parametrize("case", UNION_CASES[:3], ids=["T700", "T400_q1500", "T5"])
 def test_warp_attention_forced(sg, case):
     """The warp-level kernel stays reachable (and correct) when forced."""
     _run_case(sg, sg.ATTN_WARP, case)
 
 
-def test_auto_choice_is_the_union_kernel_at_1m(sg):
+def test_auto_choice_is_the_routed_mode_at_1m(sg):
     prm = sg.params()
-    assert sg.sgqa_attention_kernel(prm, 8192, 1040384) == sg.ATTN_TC_UNION
+    assert sg.sgqa_attention_kernel(prm, 8192, 1040384) == sg.ATTN_ROUTED
 
 
 def test_union_attention_wait_timeout_is_reported_and_recoverable(sg):
@@ -105,5 +165,28 @@ def test_union_attention_wait_timeout_is_reported_and_recoverable(sg):
         sg.sgqa_set_wait_timeout_ns(1_000_000_000)
     assert err == 5, err
     sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, res.sel_idx, res.sel_cnt, 0, out)
+    assert sg.sgqa_get_device_error() == 0
+    assert torch.equal(out, res.out)
+
+
+def test_routed_attention_wait_timeout_is_reported_and_recoverable(sg):
+    """The routed mode's launches given no time for any bounded wait: the error is
+    reported, nothing hangs, and the next call reproduces the normal output bit for bit."""
+    wl = gen.small_workload(T=256, G=2, Hg=16, B=8, k=16, planted=True)
+    inp = gen.make_inputs(wl, seed=14, device="cuda")
+    prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k, attn_kernel=sg.ATTN_ROUTED)
+    res = sg.prefill(prm, inp.q, inp.k, inp.v, inp.gate, inp.q_proxy, inp.k_proxy)
+    torch.cuda.synchronize()
+    assert sg.sgqa_get_device_error() == 0
+    ws = torch.empty(sg.sgqa_workspace_bytes(prm, sg.SGQA_OP_ATTN, wl.T, wl.T), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(inp.q)
+    sg.sgqa_set_wait_timeout_ns(0)
+    try:
+        sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, res.sel_idx, res.sel_cnt, 0, out, ws=ws)
+        err = sg.sgqa_get_device_error()
+    finally:
+        sg.sgqa_set_wait_timeout_ns(1_000_000_000)
+    assert err == 5, err
+    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, res.sel_idx, res.sel_cnt, 0, out, ws=ws)
     assert sg.sgqa_get_device_error() == 0
     assert torch.equal(out, res.out)

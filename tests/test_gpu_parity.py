@@ -201,7 +201,8 @@ def test_separate_stages_equal_fused_prefill(sg):
     ws = torch.empty(sg.sgqa_workspace_bytes(prm, sg.SGQA_OP_INDEX_TOPK, wl.T, wl.T), dtype=torch.uint8, device="cuda")
     sg.sgqa_index_topk(prm, inp.q_proxy, 0, kb, idx, cnt, ws)
     out = torch.empty_like(inp.q)
-    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, idx, cnt, 0, out)
+    ws_a = torch.empty(sg.sgqa_workspace_bytes(prm, sg.SGQA_OP_ATTN, wl.T, wl.T), dtype=torch.uint8, device="cuda")
+    sg.sgqa_sparse_attn_fwd(prm, inp.q, inp.k, inp.v, inp.gate, idx, cnt, 0, out, ws=ws_a)
     torch.cuda.synchronize()
     assert torch.equal(kb, res.k_blk) and torch.equal(idx, res.sel_idx) and torch.equal(cnt, res.sel_cnt)
     assert torch.equal(out, res.out)
@@ -289,10 +290,14 @@ def test_bounded_wait_times_out_cleanly(sg):
     _check_prefill(inp, wl, res, np.arange(wl.T))
 
 
-def test_out_of_range_selection_is_reported_not_read(sg):
+@pytest.mark.parametrize("kernel", ["union", "warp"])
+def test_out_of_range_selection_is_reported_not_read(sg, kernel):
+    """Entries outside [0, b_t] are reported and skipped by either attention kernel (forced
+    in both runs: in the routed mode a bad entry can change its unit's routing)."""
     wl = gen.small_workload(T=128, G=1, Hg=16, B=8, k=4)
     inp = _to_cuda(gen.make_inputs(wl, seed=10))
     prm = _prm(sg, wl)
+    prm.attn_kernel = sg.ATTN_TC_UNION if kernel == "union" else sg.ATTN_WARP
     res = _gpu_prefill(sg, inp, wl, prm)
     idx = res.sel_idx.clone()
     idx[0, 100, 0] = 1_000_000        # far past the cache
