@@ -37,6 +37,12 @@ constexpr int K4_D = 192;
 constexpr int K4_UNITS = K4_D / 8;            // 16-byte units per row: 24
 constexpr uint32_t K4_TILE = 16 * K4_D * 2;   // 16 keys x 192 bf16 = 6144 B
 constexpr uint32_t K4_STAGE = 2 * K4_TILE;    // K + V
+// Blocks of fewer than 8 tokens: each key row arrives by one untiled bulk copy into a
+// row of its own, padded to 400 bytes (100 words: 8 consecutive rows start 4 banks apart,
+// so an 8x8 ldmatrix of 16-byte row pieces touches every bank once, without a swizzle).
+constexpr uint32_t K4_ROW = 400;
+__host__ __device__ constexpr uint32_t k4_tile_bytes(bool tma) { return tma ? K4_TILE : 16 * K4_ROW; }
+__host__ __device__ constexpr uint32_t k4_stage_bytes(bool tma) { return 2 * k4_tile_bytes(tma); }
 constexpr int K4_SEL_CACHE = 512;             // selection entries a warp keeps in shared memory
 
 struct K4Args {
@@ -90,12 +96,13 @@ __global__ void __launch_bounds__(NW * 32, 1)
     k4_sparse_attn(const __grid_constant__ K4Args a, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV) {
   constexpr int NSTAGE = 2;  // a stage in flight while the other is consumed
+  constexpr uint32_t TILE = k4_tile_bytes(TMA), STAGE = k4_stage_bytes(TMA);
   extern __shared__ uint8_t k4_smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(k4_smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = lane_id();
-  const uint32_t wbase = smem_u32(smem) + warp * (NSTAGE * K4_STAGE);
-  const uint32_t bar0 = smem_u32(smem) + NW * NSTAGE * K4_STAGE + warp * NSTAGE * 8;
+  const uint32_t wbase = smem_u32(smem) + warp * (NSTAGE * STAGE);
+  const uint32_t bar0 = smem_u32(smem) + NW * NSTAGE * STAGE + warp * NSTAGE * 8;
 
   const int64_t n_units = (int64_t)a.G * a.rows * a.nsplit;
   int64_t unit = (int64_t)blockIdx.x * NW + warp;
@@ -132,7 +139,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   // Block j of the selection: -1 past the count, -2 for an index outside 0..bt.  Rows of
   // up to K4_SEL_CACHE entries are copied once into this warp's shared-memory table, so a
   // lookup is one broadcast shared load; longer rows read the global array.
-  int32_t* selc = reinterpret_cast<int32_t*>(smem + NW * NSTAGE * K4_STAGE + NW * NSTAGE * 8) + warp * K4_SEL_CACHE;
+  int32_t* selc = reinterpret_cast<int32_t*>(smem + NW * NSTAGE * STAGE + NW * NSTAGE * 8) + warp * K4_SEL_CACHE;
   const uint32_t selc_s = smem_u32(selc);
   const bool cached = !a.dense && cnt <= K4_SEL_CACHE;
   if (cached) {
@@ -179,7 +186,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
   }
   __syncwarp();
 
-  if (TMA && lane == 0) {
+  if (lane == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
@@ -196,13 +203,18 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
   for (int jx = 0; jx < 4; ++jx)
     v_off[jx] = ((lane >> 3) & 1) * 3072 + kr * 128 + (((((lane >> 4) ^ kr)) ^ (2u * jx)) << 4);
+  // the padded-row layout (blocks of fewer than 8 tokens): byte n * K4_ROW + 16 u
+  const uint32_t k_pad = kr * K4_ROW + (lane >> 3) * 16;
+  const uint32_t v_pad = ((lane >> 3) & 1) * 8 * K4_ROW + kr * K4_ROW + (lane >> 4) * 16;
 
   // ---- stage loader.  TMA: lane 0 fetches stage s from blocks (b0, b1) looked up one
-  // iteration earlier, so no shuffle latency sits in front of the copies. ----
+  // iteration earlier, so no shuffle latency sits in front of the copies.  Blocks of fewer
+  // than 8 tokens: lane l copies key l & 15 of K (l < 16) or V with one bulk copy.  Both
+  // complete on the stage's mbarrier. ----
   auto issue = [&](int32_t s, int32_t b0, int32_t b1) {
     const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
-    const uint32_t ks_addr = wbase + slot * K4_STAGE;
-    const uint32_t vs_addr = ks_addr + K4_TILE;
+    const uint32_t ks_addr = wbase + slot * STAGE;
+    const uint32_t vs_addr = ks_addr + TILE;
     if (TMA) {
       // B = 8: two blocks of 8 keys; B = 16: the two halves of one block
       if (b0 < 0) b0 = bt;  // unused / invalid slot: fetch the own block, masked below
@@ -219,18 +231,17 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     } else {
       const int64_t row_lim = (int64_t)a.G * a.ctx_cap - 1;
-      for (int w = lane; w < 16 * K4_UNITS; w += 32) {
-        const uint32_t n = w / K4_UNITS, u = w % K4_UNITS;
-        const int32_t j = s * bps + (int32_t)n / a.B;
-        int64_t b = j < cnt ? (a.dense ? j : __ldg(sel + j)) : -1;
-        if (b < 0 || b > bt) b = bt;
-        int64_t row = row_base + b * a.B + (n % a.B);
-        if (row > row_lim) row = row_lim;
-        const uint32_t off = k4_kv_off(n, u);
-        cp_async_16(ks_addr + off, a.kc + row * K4_D + u * 8);
-        cp_async_16(vs_addr + off, a.vc + row * K4_D + u * 8);
-      }
-      cp_async_commit();
+      const uint32_t bar = bar0 + 8 * slot;
+      if (lane == 0) mbar_arrive_expect_tx(bar, STAGE - 2 * 16 * (K4_ROW - K4_D * 2));
+      __syncwarp();
+      const uint32_t n = lane & 15;
+      const int32_t j = s * bps + (int32_t)n / a.B;
+      int64_t b = j < cnt ? (a.dense ? j : __ldg(sel + j)) : -1;
+      if (b < 0 || b > bt) b = bt;  // unused / invalid slot: a valid row, masked below
+      int64_t row = row_base + b * a.B + (n % a.B);
+      if (row > row_lim) row = row_lim;
+      bulk_load_g2s((lane < 16 ? ks_addr : vs_addr) + n * K4_ROW, (lane < 16 ? a.kc : a.vc) + row * K4_D, K4_D * 2,
+                    bar);
     }
   };
 
@@ -246,13 +257,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
   int32_t issued = s_begin;
 
   auto wait_stage = [&](int32_t s) -> bool {
-    if (TMA) {
-      const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
-      return mbar_wait(bar0 + 8 * slot, (uint32_t)((s - s_begin) / NSTAGE) & 1u, a.wait_ns);
-    }
-    cp_async_wait<NSTAGE - 1>();
-    __syncwarp();
-    return true;
+    const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
+    return mbar_wait(bar0 + 8 * slot, (uint32_t)((s - s_begin) / NSTAGE) & 1u, a.wait_ns);
   };
 
   // nb0/nb1: blocks of the stage issued last (masked by the next iteration); pb0/pb1:
@@ -270,8 +276,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
     nb0 = pb0;
     nb1 = pb1;
     issued = s_begin + 1;
-  } else if (!TMA) {
-    cp_async_commit();
   }
   look_stage(s_begin + 1);
 
@@ -285,8 +289,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
       nb1 = pb1;
       issued = s + 2;
       look_stage(s + 2);
-    } else if (!TMA) {
-      cp_async_commit();
     }
     bool fast = true;
     if (TMA) {
@@ -299,8 +301,8 @@ __global__ void __launch_bounds__(NW * 32, 1)
       }
     }
     if (!wait_stage(s)) { ok = false; break; }
-    const uint32_t ks_addr = wbase + ((uint32_t)(s - s_begin) % NSTAGE) * K4_STAGE;
-    const uint32_t vs_addr = ks_addr + K4_TILE;
+    const uint32_t ks_addr = wbase + ((uint32_t)(s - s_begin) % NSTAGE) * STAGE;
+    const uint32_t vs_addr = ks_addr + TILE;
 
     // ---- S = Q K^T: two n-tiles x 12 k-steps as four independent chains ----
     float sc[2][4];
@@ -316,7 +318,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(((kp & 2) ? khi : klo) + nt * 3072 + (kp >> 2) * 1024, b0, b1, b2, b3);
+          if (TMA)
+            ldsm_x4(((kp & 2) ? khi : klo) + nt * 3072 + (kp >> 2) * 1024, b0, b1, b2, b3);
+          else
+            ldsm_x4(ks_addr + k_pad + nt * 8 * K4_ROW + kp * 32, b0, b1, b2, b3);
           mma_bf16_16816(acc[nt][0], qa[kp], b0, b1);
           mma_bf16_16816(acc[nt][1], qa[kp + 1], b2, b3);
         }
@@ -399,7 +404,10 @@ __global__ void __launch_bounds__(NW * 32, 1)
 #pragma unroll
     for (int dp = 0; dp < 12; ++dp) {
       uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vs_addr + v_off[dp & 3] + (dp >> 2) * 1024, v0, v1, v2, v3);
+      if (TMA)
+        ldsm_x4_t(vs_addr + v_off[dp & 3] + (dp >> 2) * 1024, v0, v1, v2, v3);
+      else
+        ldsm_x4_t(vs_addr + v_pad + dp * 32, v0, v1, v2, v3);
       mma_bf16_16816(o[2 * dp], pa, v0, v1);
       mma_bf16_16816(o[2 * dp + 1], pa, v2, v3);
     }
@@ -408,7 +416,7 @@ __global__ void __launch_bounds__(NW * 32, 1)
 
   if (!ok) {
     // drain the copies still in flight into this warp's slots, then leave
-    if (TMA && lane == 0) {
+    if (lane == 0) {
       for (int32_t s = issued - NSTAGE > s_begin ? issued - NSTAGE : s_begin; s < issued; ++s) {
         const uint32_t slot = (uint32_t)(s - s_begin) % NSTAGE;
         mbar_wait(bar0 + 8 * slot, (uint32_t)((s - s_begin) / NSTAGE) & 1u, kDrainLimitNs);
@@ -417,7 +425,6 @@ __global__ void __launch_bounds__(NW * 32, 1)
     __syncwarp();
     return;
   }
-  if (!TMA) cp_async_wait<0>();
   __syncwarp();
 
   // full row sums across the quad

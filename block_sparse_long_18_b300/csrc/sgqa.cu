@@ -149,12 +149,14 @@ cudaError_t ensure_smem_attr(AttrKernel which, const void* fn, size_t bytes) {
 
 // ---- attention launch: 8 warps (units) per CTA, two stages each ----
 constexpr int kK4Warps = 8;
-size_t k4_smem(int nw) { return (size_t)nw * 2 * K4_STAGE + (size_t)nw * 2 * 8 + (size_t)nw * K4_SEL_CACHE * 4 + 1024; }
+size_t k4_smem(int nw, bool tma) {
+  return (size_t)nw * 2 * k4_stage_bytes(tma) + (size_t)nw * 2 * 8 + (size_t)nw * K4_SEL_CACHE * 4 + 1024;
+}
 
 template <bool TMA>
 cudaError_t launch_k4_t(const K4Args& a, const CUtensorMap& tk, const CUtensorMap& tv, int64_t n_units,
                         cudaStream_t st) {
-  const size_t smem = k4_smem(kK4Warps);
+  const size_t smem = k4_smem(kK4Warps, TMA);
   const cudaError_t e = ensure_smem_attr(TMA ? kAttrK4Tma : kAttrK4Cp,
                                          reinterpret_cast<const void*>(k4_sparse_attn<kK4Warps, TMA>), smem);
   if (e != cudaSuccess) return e;
@@ -922,7 +924,8 @@ static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64
   }
   const size_t need = sgqa_workspace_bytes(prm, SGQA_OP_DECODE, 1, max_len, batch);
   if (!ws || ws_bytes < need) return SGQA_ERR_WORKSPACE_TOO_SMALL;
-  if (!aligned16(ws) || !aligned16(q_proxy) || !aligned16(k_blk_cache) || !aligned16(q) || !aligned16(out))
+  if (!aligned16(ws) || !aligned16(q_proxy) || !aligned16(k_blk_cache) || !aligned16(q) || !aligned16(out) ||
+      !aligned16(k_cache) || !aligned16(v_cache))
     return SGQA_ERR_INVALID_ARGUMENT;
   const int64_t nb_total = total / p.B;
   const int64_t max_cand = (max_len - 1) / p.B;
