@@ -506,7 +506,8 @@ def run_sgqa(args, rank, world, local_rank):
 
     # K1 once, K2 + top-k per 8,192-row pass (top-k in two launches for rows past 16,384
     # candidates: per-slice selection, then the merge), K4 once
-    launches_per_step = 2
+    # (the routed attention: two routing launches and the warp-level kernel besides the union one)
+    launches_per_step = 2 + (3 if sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start) == sgqa.ATTN_ROUTED else 0)
     for r0 in range(0, wl.T, 8192):
         cand_last = (wl.q_start + min(wl.T, r0 + 8192) - 1) // wl.B
         launches_per_step += (1 if cand_last > 0 else 0) + (2 if cand_last > 16384 and wl.k > 1 else 1)
