@@ -37,7 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline per stage"
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
-K4_KERNEL = {1: "k4_sparse_attn", 2: "k4u_sparse_attn", 3: "k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn"}
+K4_KERNEL = {1: "k4_sparse_attn", 2: "k4u_sparse_attn", 3: "k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn",
+             4: "k4g_group + k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn"}
 
 
 def load_peaks():
@@ -81,20 +82,84 @@ def work_model(wl):
     return w
 
 
-def selection_stats(plan, wl, units_per_pass=4096):
+_I64_MIN = -(1 << 63)
+
+
+def _lsr(x, s):
+    """Logical right shift of int64 tensors holding 64-bit patterns."""
+    return (x >> s) & ((1 << (64 - s)) - 1)
+
+
+def _splitmix(x):
+    """The splitmix64 output function on int64 tensors (wrap-around arithmetic), as the
+    library's grouping kernel applies it."""
+    c1 = 0xbf58476d1ce4e5b9 - (1 << 64)
+    c2 = 0x94d049bb133111eb - (1 << 64)
+    x = x ^ _lsr(x, 30)
+    x = x * c1
+    x = x ^ _lsr(x, 27)
+    x = x * c2
+    return x ^ _lsr(x, 31)
+
+
+GROUP_WINDOW = 4096  # rows per grouping window of the library's grouped attention mode
+
+
+def grouped_row_order(sel, cnt, wl, win=GROUP_WINDOW):
+    """The grouped attention mode's row order, restated with torch for the benchmark's
+    routing statistics: per group and window of `win` rows, the rows sorted by (high 32 bits
+    of the least splitmix64 hash of their selected blocks, 22 bits of a second such hash,
+    row).  Returns perm [G, T] (the row at each slot)."""
+    G, T, k = sel.shape
+    dev = sel.device
+    perm = torch.empty((G, T), dtype=torch.int64, device=dev)
+    i = torch.arange(T, device=dev)
+    bt = (wl.q_start + i) // wl.B
+    cap = torch.clamp(bt + 1, max=k)
+    j = torch.arange(k, device=dev)
+    for g in range(G):
+        c = cnt[g].long()
+        c = torch.where(c < 1, torch.ones_like(c), torch.minimum(c, cap))
+        b = sel[g].long()
+        valid = (j[None, :] < c[:, None]) & (b >= 0) & (b <= bt[:, None])
+        big = torch.full_like(b, (1 << 63) - 1)
+        h1 = torch.where(valid, _splitmix(b) ^ _I64_MIN, big).amin(dim=1) ^ _I64_MIN
+        h2 = torch.where(valid, _splitmix(b ^ 0x5bd1e9955bd1e995) ^ _I64_MIN, big).amin(dim=1) ^ _I64_MIN
+        row_bits = win.bit_length() - 1
+        key = (h1 & -(1 << 32)) | (_lsr(h2, 32 + row_bits) << row_bits) | (i % win)
+        nwin = (T + win - 1) // win
+        pad = nwin * win - T
+        keyw = torch.cat([key ^ _I64_MIN, torch.full((pad,), (1 << 63) - 1, device=dev, dtype=torch.int64)])
+        srt, _ = torch.sort(keyw.view(nwin, win), dim=1)
+        order = ((srt ^ _I64_MIN) & (win - 1)) + torch.arange(nwin, device=dev)[:, None] * win
+        perm[g] = order.reshape(-1)[:T]
+        del b, valid, big
+    return perm
+
+
+def selection_stats(plan, wl, units_per_pass=4096, grouped=False):
     """From the step's selection: how many distinct (group, block) pairs some row selected
-    (the K/V every attention kernel must read at least once), and for units of 8 query rows
-    the size of each union and the 128-key chunks the union kernel runs over it."""
+    (the K/V every attention kernel must read at least once), and for units of 8 rows (8
+    consecutive rows, or with grouped=True the grouped mode's units) the size of each
+    union, the library's routing of the unit, and the MMA work each kernel issues."""
     if wl.T % 8:
         return None
     sel = plan.sel_idx  # [G, T, k], ascending, -1 padded
+    cnt_rows = plan.sel_cnt
     G, T, k = sel.shape
+    if grouped:
+        perm = grouped_row_order(sel, cnt_rows, wl)
+        sel = torch.stack([sel[g][perm[g]] for g in range(G)])
+        cnt_rows = torch.stack([cnt_rows[g][perm[g]] for g in range(G)])
     nb = (wl.q_start + wl.T + wl.B - 1) // wl.B
     used = torch.zeros((G, nb + 1), dtype=torch.bool, device=sel.device)
     chunks = r_chunks = r_stages = r_union = r_warp = 0
     blocks = 0
-    units = sel.view(G, T // 8, 8 * k)
-    cnt = plan.sel_cnt.view(G, T // 8, 8).sum(dim=-1)  # (row, block) pairs per unit
+    units = sel.reshape(G, T // 8, 8 * k)
+    cnt = cnt_rows.reshape(G, T // 8, 8).sum(dim=-1)  # (row, block) pairs per unit
+    # the largest own block of each unit (windows of 16,384 blocks it spans)
+    pos = wl.q_start + (perm if grouped else torch.arange(T, device=sel.device).expand(G, T))
+    bmax = (pos // wl.B).reshape(G, T // 8, 8).amax(dim=-1)
     for u0 in range(0, T // 8, units_per_pass):
         part = units[:, u0:u0 + units_per_pass]
         srt, _ = torch.sort(part, dim=-1)
@@ -103,15 +168,13 @@ def selection_stats(plan, wl, units_per_pass=4096):
         new[..., 1:] &= srt[..., 1:] != srt[..., :-1]
         nu = new.sum(dim=-1)  # [G, units]: distinct blocks
         pairs = cnt[:, u0:u0 + units_per_pass]
-        # the library's routing rule: union iff 100 * windows * |union| <= 55 * pairs, windows
-        # = the 16,384-block windows the unit's own blocks reach
-        last_row = torch.clamp(torch.arange(u0, u0 + pairs.shape[1], device=sel.device) * 8 + 7, max=T - 1)
-        windows = (wl.q_start + last_row) // wl.B // 16384 + 1
-        to_union = 100 * windows[None, :] * nu <= 55 * pairs
+        # the library's routing rule: union iff 100 * windows * |union| <= 55 * pairs
+        windows = bmax[:, u0:u0 + units_per_pass] // 16384 + 1
+        to_union = 100 * windows * nu <= 55 * pairs
         blocks += int(nu.sum())
         chunks += int(((nu + 15) // 16).sum())
         r_chunks += int(((nu + 15) // 16)[to_union].sum())
-        r_stages += int(((plan.sel_cnt.view(G, T // 8, 8)[:, u0:u0 + units_per_pass] + 1) // 2)[~to_union].sum())
+        r_stages += int(((cnt_rows.reshape(G, T // 8, 8)[:, u0:u0 + units_per_pass] + 1) // 2)[~to_union].sum())
         r_union += int(to_union.sum())
         r_warp += int((~to_union).sum())
         for g in range(G):
@@ -389,7 +452,8 @@ def run_sgqa(args, rank, world, local_rank):
     # ---- roofline of each stage (survey's per-stage line: max of FLOPs at the bf16 peak and
     # algorithmic bytes at the HBM peak, both measured on the B300s) ----
     w = work_model(wl)
-    sel_stats = selection_stats(plan, wl)
+    attn_kind = sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start)
+    sel_stats = selection_stats(plan, wl, grouped=attn_kind == sgqa.ATTN_GROUPED)
     if sel_stats is not None:
         w["k4_kv_once_bytes"] = sel_stats["kv_blocks_selected"] * 2 * 2 * wl.D * wl.B
     k4_compulsory = w["k4_rows_bytes"] + w["k4_kv_once_bytes"]
@@ -424,7 +488,7 @@ def run_sgqa(args, rank, world, local_rank):
     k4s["per_row_gather_bytes"] = w["k4_gather_bytes"] + w["k4_rows_bytes"]
     k4s["per_row_gather_frac_of_hbm"] = round(k4s["per_row_gather_bytes"] / (k4_ms / 1e3) / hbm_bps, 4)
     k4_kernel = K4_KERNEL.get(sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start), "k4_sparse_attn")
-    if sel_stats is not None and k4_kernel.startswith("k4r_count"):
+    if sel_stats is not None and ("k4r_count" in k4_kernel):
         # routed: units whose union is small go to the union kernel, the rest to the
         # warp-level kernel (16 heads x 16 keys x 192 x 4 per stage of two blocks)
         issued = (sel_stats["routed_union_chunks"] * 128 * 128 * wl.D * 4
@@ -506,8 +570,10 @@ def run_sgqa(args, rank, world, local_rank):
 
     # K1 once, K2 + top-k per 8,192-row pass (top-k in two launches for rows past 16,384
     # candidates: per-slice selection, then the merge), K4 once
-    # (the routed attention: two routing launches and the warp-level kernel besides the union one)
-    launches_per_step = 2 + (3 if sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start) == sgqa.ATTN_ROUTED else 0)
+    # (the routed attention: two routing launches and the warp-level kernel besides the union
+    # one; the grouped mode one more for the row order)
+    kind = sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start)
+    launches_per_step = 2 + {sgqa.ATTN_ROUTED: 3, sgqa.ATTN_GROUPED: 4}.get(kind, 0)
     for r0 in range(0, wl.T, 8192):
         cand_last = (wl.q_start + min(wl.T, r0 + 8192) - 1) // wl.B
         launches_per_step += (1 if cand_last > 0 else 0) + (2 if cand_last > 16384 and wl.k > 1 else 1)

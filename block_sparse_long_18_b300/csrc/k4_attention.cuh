@@ -69,6 +69,7 @@ struct K4Args {
   // + tile of 8 rows), one warp per row, for b < *n_units_dev
   const int32_t* units;
   const int32_t* n_units_dev;
+  const int32_t* perm;  // grouped units: perm[g * rows + s] is the row at slot s (null: s itself)
   uint64_t wait_ns;
   int64_t pos[256];
   int64_t kv_off[256];
@@ -111,8 +112,9 @@ __global__ void __launch_bounds__(NW * 32, 1)
     if ((int64_t)blockIdx.x >= (int64_t)*a.n_units_dev) return;
     const int64_t ntiles = (a.rows + 7) / 8;
     const int64_t uid = __ldg(a.units + blockIdx.x);
-    const int64_t row = (uid % ntiles) * 8 + warp;
-    if (row >= a.rows) return;
+    const int64_t slot = (uid % ntiles) * 8 + warp;
+    if (slot >= a.rows) return;
+    const int64_t row = a.perm ? (int64_t)__ldg(a.perm + (uid / ntiles) * a.rows + slot) : slot;
     unit = (uid / ntiles) * a.rows + row;
   }
   if (unit >= n_units) return;

@@ -31,6 +31,7 @@ constexpr int kRouteUnionCost = SGQA_ROUTE_UNION_COST, kRoutePairCost = SGQA_ROU
 struct K4RouteArgs {
   const int32_t* sel_idx;  // [G, rows, kcap]
   const int32_t* sel_cnt;  // [G, rows]
+  const int32_t* perm;     // [G, rows] row at each slot (grouped units), or null: slot = row
   int32_t* choice;         // [G * tiles]: 1 = union kernel, 0 = warp-level kernel
   int32_t* union_units;    // [G * tiles] (k4r_compact)
   int32_t* warp_units;     // [G * tiles] (k4r_compact)
@@ -50,8 +51,10 @@ __global__ void __launch_bounds__(K4R_WARPS * 32) k4r_count(const K4RouteArgs a)
   const int64_t i0 = (u % ntiles) * 8;
   uint32_t* bm = seen[warp];
   int32_t cnt_l = 0, bt_l = -1;
+  int64_t row_l = 0;
   if (lane < 8 && i0 + lane < a.rows) {
-    const int64_t i = i0 + lane;
+    const int64_t i = a.perm ? (int64_t)__ldg(a.perm + (int64_t)g * a.rows + i0 + lane) : i0 + lane;
+    row_l = i;
     bt_l = (int32_t)((a.pos0 + i) >> 3);
     int32_t c = __ldg(a.sel_cnt + (int64_t)g * a.rows + i);
     const int32_t cap = a.kcap < bt_l + 1 ? a.kcap : bt_l + 1;
@@ -72,7 +75,8 @@ __global__ void __launch_bounds__(K4R_WARPS * 32) k4r_count(const K4RouteArgs a)
 #pragma unroll 1
     for (int r = 0; r < 8; ++r) {
       const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r), bt = __shfl_sync(0xffffffffu, bt_l, r);
-      const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i0 + r) * a.kcap;
+      const int64_t row = __shfl_sync(0xffffffffu, row_l, r);
+      const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + row) * a.kcap;
       for (int32_t j = (int32_t)lane; j < cnt; j += 32) {
         const int32_t b = __ldg(sel + j);
         const int32_t o = b - wb;
@@ -138,6 +142,96 @@ __global__ void __launch_bounds__(K4R_COMPACT_THREADS) k4r_compact(const K4Route
     a.counts[0] = (int32_t)tu;
     a.counts[1] = (int32_t)tw;
   }
+}
+
+
+// ---------------------------------------------------------------------------------------
+// Grouped units: one CTA of K4G_THREADS threads per (group, window of K4G_WIN rows).
+// ---------------------------------------------------------------------------------------
+#ifndef SGQA_GROUP_WINDOW
+#define SGQA_GROUP_WINDOW 4096
+#endif
+constexpr int K4G_WIN = SGQA_GROUP_WINDOW;   // rows per grouping window (a power of 2, >= 1024)
+constexpr int K4G_THREADS = 1024;
+static_assert(K4G_WIN >= K4G_THREADS && (K4G_WIN & (K4G_WIN - 1)) == 0, "grouping window");
+
+// The splitmix64 output function (Steele, Lea and Flood, "Fast splittable pseudorandom
+// number generators", 2014): a bijective 64-bit mixer.
+__device__ __forceinline__ uint64_t k4g_mix(uint64_t x) {
+  x ^= x >> 30;
+  x *= 0xbf58476d1ce4e5b9ull;
+  x ^= x >> 27;
+  x *= 0x94d049bb133111ebull;
+  x ^= x >> 31;
+  return x;
+}
+
+struct K4GroupArgs {
+  const int32_t* sel_idx;  // [G, rows, kcap]
+  const int32_t* sel_cnt;  // [G, rows]
+  int32_t* perm;           // [G, rows]
+  int64_t rows, pos0;
+  int32_t G, kcap;
+};
+
+__global__ void __launch_bounds__(K4G_THREADS) k4g_group(const K4GroupArgs a) {
+  __shared__ uint64_t key[K4G_WIN];
+  const int64_t nwin = (a.rows + K4G_WIN - 1) / K4G_WIN;
+  const int32_t g = (int32_t)(blockIdx.x / nwin);
+  const int64_t w0 = (int64_t)(blockIdx.x % nwin) * K4G_WIN;
+  const int nrow = (int)(a.rows - w0 < K4G_WIN ? a.rows - w0 : K4G_WIN);
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  // signature of row w0 + r, one warp per row; the same entry rules as the union builder
+  for (int r = (int)warp; r < K4G_WIN; r += K4G_THREADS / 32) {
+    uint64_t h1 = ~0ull, h2 = ~0ull;
+    if (r < nrow) {
+      const int64_t i = w0 + r;
+      const int32_t bt = (int32_t)((a.pos0 + i) >> 3);
+      int32_t c = __ldg(a.sel_cnt + (int64_t)g * a.rows + i);
+      const int32_t cap = a.kcap < bt + 1 ? a.kcap : bt + 1;
+      if (c < 1 || c > cap) c = c < 1 ? 1 : cap;
+      const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i) * a.kcap;
+      for (int32_t j = (int32_t)lane; j < c; j += 32) {
+        const int32_t b = __ldg(sel + j);
+        if (b < 0 || b > bt) continue;
+        const uint64_t x = k4g_mix((uint64_t)(uint32_t)b);
+        h1 = x < h1 ? x : h1;
+        const uint64_t y = k4g_mix((uint64_t)(uint32_t)b ^ 0x5bd1e9955bd1e995ull);
+        h2 = y < h2 ? y : h2;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const uint64_t x = __shfl_xor_sync(0xffffffffu, h1, o), y = __shfl_xor_sync(0xffffffffu, h2, o);
+        h1 = x < h1 ? x : h1;
+        h2 = y < h2 ? y : h2;
+      }
+    }
+    // sort key: high 32 bits of the first hash, then bits of the second, then the row
+    constexpr int kRowBits = __builtin_ctz(K4G_WIN);
+    if (lane == 0)
+      key[r] = r < nrow ? ((h1 & 0xFFFFFFFF00000000ull) | ((h2 >> (32 + kRowBits)) << kRowBits) | (uint64_t)r)
+                        : ~0ull;
+  }
+  __syncthreads();
+  // bitonic sort of the window's keys, ascending (thread t owns elements t, t + 1024, ...)
+  for (uint32_t k = 2; k <= (uint32_t)K4G_WIN; k <<= 1) {
+    for (uint32_t j = k >> 1; j > 0; j >>= 1) {
+      for (uint32_t t = threadIdx.x; t < (uint32_t)K4G_WIN; t += K4G_THREADS) {
+        const uint32_t p = t ^ j;
+        if (p > t) {
+          const uint64_t x = key[t], y = key[p];
+          const bool up = (t & k) == 0;
+          if ((x > y) == up) {
+            key[t] = y;
+            key[p] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  for (uint32_t t = threadIdx.x; (int)t < nrow; t += K4G_THREADS)
+    a.perm[(int64_t)g * a.rows + w0 + t] = (int32_t)(w0 + (int64_t)(key[t] & (K4G_WIN - 1)));
 }
 
 }  // namespace sgqa

@@ -79,9 +79,11 @@ struct K4UArgs {
   int32_t gate_per_dim;
   uint64_t wait_ns;
   // routed mode: the units to serve are units[0 .. *n_units_dev) (unit = g * tiles + tile
-  // of 8 rows); otherwise every unit of the call
+  // of 8 slots); otherwise every unit of the call
   const int32_t* units;
   const int32_t* n_units_dev;
+  // grouped units: perm[g * rows + s] is the row at slot s (null: slot s is row s)
+  const int32_t* perm;
 };
 
 __global__ void __launch_bounds__(K4U_THREADS, 1)
@@ -103,6 +105,10 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
   // units of this launch: every (group, 8-row tile), or the routed list
   const int64_t n_units = a.units ? (int64_t)*a.n_units_dev : (int64_t)a.G * ntiles;
   auto unit_id = [&](int64_t u) -> int64_t { return a.units ? (int64_t)__ldg(a.units + u) : u; };
+  // row at slot s of group g; a.rows (no row) for the empty slots of a ragged last tile
+  auto row_at = [&](int32_t g, int64_t s) -> int64_t {
+    return s >= a.rows ? a.rows : (a.perm ? (int64_t)__ldg(a.perm + (int64_t)g * a.rows + s) : s);
+  };
   auto tbl = [&](uint32_t buf) { return smem + K4U_T_OFF + buf * K4U_TB; };
 
   if (threadIdx.x == 0) {
@@ -162,8 +168,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       uint32_t* rbits = reinterpret_cast<uint32_t*>(T + K4U_TB_RBITS);
       int32_t* meta = reinterpret_cast<int32_t*>(T + K4U_TB_META);
       int32_t cnt_l = 0, bt_l = -1;
+      const int64_t row_l = row_at(g, i0 + (lane & 7));  // lanes 0..7: the unit's rows
       if (lane < 8 && i0 + lane < a.rows) {
-        const int64_t i = i0 + lane;
+        const int64_t i = row_l;
         bt_l = (int32_t)((a.pos0 + i) >> 3);
         int32_t c = __ldg(a.sel_cnt + (int64_t)g * a.rows + i);
         const int32_t cap = a.kcap < bt_l + 1 ? a.kcap : bt_l + 1;
@@ -188,7 +195,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r0 + rr);
-            const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i0 + r0 + rr) * a.kcap;
+            const int64_t row = __shfl_sync(0xffffffffu, row_l, r0 + rr);
+            const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + row) * a.kcap;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const int32_t j = (int32_t)lane + 32 * k;
@@ -242,7 +250,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r0 + rr);
-            const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i0 + r0 + rr) * a.kcap;
+            const int64_t row = __shfl_sync(0xffffffffu, row_l, r0 + rr);
+            const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + row) * a.kcap;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
               const int32_t j = (int32_t)lane + 32 * k;
@@ -423,7 +432,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     auto write_q = [&](int64_t u) {  // this half of the Q rows of unit u -> tensor memory
       const int64_t uid = unit_id(u);
       const int32_t g = (int32_t)(uid / ntiles);
-      const int64_t i = (uid % ntiles) * 8 + r;
+      const int64_t i = row_at(g, (uid % ntiles) * 8 + r);
       const bool valid = i < a.rows;
       const uint4* src =
           reinterpret_cast<const uint4*>(a.q + ((i * a.H) + (int64_t)g * 16 + h) * K4U_D + 96 * hf);
@@ -481,7 +490,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       if (sync_stop()) break;
       const int64_t uid = unit_id(u);
       const int32_t g = (int32_t)(uid / ntiles);
-      const int64_t i = (uid % ntiles) * 8 + r;
+      const int64_t i = row_at(g, (uid % ntiles) * 8 + r);
       const bool row_ok = i < a.rows;
       const uint8_t* T = tbl(buf);
       const uint32_t* rb = reinterpret_cast<const uint32_t*>(T + K4U_TB_RBITS);
@@ -498,7 +507,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       // chunk loop: this warp serves query row rr of the unit (TMEM lanes 16 rr .. 16 rr + 15);
       // thread t holds heads hA = t/4 and hB = hA + 8, keys kq, kq + 1 of every block
       const uint32_t* rb_row = rb + rr * (K4U_MAXU / 32);
-      const int64_t ir = (uid % ntiles) * 8 + rr;
+      const int64_t ir = row_at(g, (uid % ntiles) * 8 + rr);
       const int32_t own_r = meta[1 + rr];
       const int32_t tlim_r = (int32_t)((a.pos0 + ir) & 7);
       float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;

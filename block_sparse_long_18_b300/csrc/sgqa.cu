@@ -61,7 +61,7 @@ sgqa_status check_params(const sgqa_params* p, Prm& o) {
   if (B != 1 && B != 2 && B != 4 && B != 8 && B != 16) return SGQA_ERR_UNSUPPORTED_SHAPE;
   if (p->gate_per_dim != 0 && p->gate_per_dim != 1) return SGQA_ERR_INVALID_ARGUMENT;
   if (p->attn_kernel != SGQA_ATTN_AUTO && p->attn_kernel != SGQA_ATTN_WARP && p->attn_kernel != SGQA_ATTN_TC_UNION &&
-      p->attn_kernel != SGQA_ATTN_ROUTED)
+      p->attn_kernel != SGQA_ATTN_ROUTED && p->attn_kernel != SGQA_ATTN_GROUPED)
     return SGQA_ERR_INVALID_ARGUMENT;
   o.G = p->num_kv_groups;
   o.Hg = p->heads_per_group;
@@ -365,18 +365,24 @@ bool union_fits(const Prm& p, int32_t dense, int64_t T, int64_t q_start) {
 int attn_choice(const Prm& p, int32_t dense, int64_t T, int64_t q_start, bool ws_ok) {
   const bool fits = union_fits(p, dense, T, q_start);
   switch (p.attn_kernel) {
-    case SGQA_ATTN_AUTO: return fits ? (ws_ok ? SGQA_ATTN_ROUTED : SGQA_ATTN_TC_UNION) : SGQA_ATTN_WARP;
+    case SGQA_ATTN_AUTO:
+      // (the routing rule sends no unit to the union kernel once every unit spans more
+      // windows than kRoutePairCost * 8 / kRouteUnionCost: then the warp-level kernel alone)
+      if (fits && (q_start / 8) / K4U_WIN + 1 > (int64_t)kRoutePairCost * 8 / kRouteUnionCost) return SGQA_ATTN_WARP;
+      return fits ? (ws_ok ? SGQA_ATTN_GROUPED : SGQA_ATTN_TC_UNION) : SGQA_ATTN_WARP;
     case SGQA_ATTN_WARP: return SGQA_ATTN_WARP;
     case SGQA_ATTN_TC_UNION: return fits ? SGQA_ATTN_TC_UNION : -1;
     case SGQA_ATTN_ROUTED: return fits ? SGQA_ATTN_ROUTED : -1;
+    case SGQA_ATTN_GROUPED: return fits ? SGQA_ATTN_GROUPED : -1;
   }
   return -1;
 }
 
-// Workspace of the routed attention mode for T query rows: the per-unit choice, the two
-// unit lists and their lengths (units = G x ceil(T / 8)).
+// Workspace of the routed and grouped attention modes for T query rows: the per-unit
+// choice, the two unit lists and their lengths (units = G x ceil(T / 8)), and the grouped
+// mode's row order [G, T].
 struct AttnWs {
-  size_t choice, union_units, warp_units, counts, total;
+  size_t choice, union_units, warp_units, counts, perm, total;
 };
 AttnWs attn_ws_layout(const Prm& p, int64_t T) {
   AttnWs w{};
@@ -385,7 +391,8 @@ AttnWs attn_ws_layout(const Prm& p, int64_t T) {
   w.union_units = align_up(nu * 4, 256);
   w.warp_units = w.union_units + align_up(nu * 4, 256);
   w.counts = w.warp_units + align_up(nu * 4, 256);
-  w.total = w.counts + 256;
+  w.perm = w.counts + 256;
+  w.total = w.perm + align_up((size_t)p.G * (size_t)std::max<int64_t>(T, 0) * 4, 256);
   return w;
 }
 
@@ -406,17 +413,34 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
   const bool ws_ok = ws && aligned16(ws) && ws_bytes >= wl.total;
   const int kernel = attn_choice(p, dense, T, q_start, ws_ok);
   if (kernel < 0) return SGQA_ERR_UNSUPPORTED_SHAPE;
-  if (kernel == SGQA_ATTN_ROUTED && !ws_ok) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  const bool routed = kernel == SGQA_ATTN_ROUTED || kernel == SGQA_ATTN_GROUPED;
+  if (routed && !ws_ok) return SGQA_ERR_WORKSPACE_TOO_SMALL;
   const uint64_t kv_rows = (uint64_t)p.G * ctx_cap;
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int32_t* union_units = nullptr;
   const int32_t* counts = nullptr;
-  if (kernel == SGQA_ATTN_ROUTED) {
+  const int32_t* perm = nullptr;
+  if (kernel == SGQA_ATTN_GROUPED) {
+    // rows ordered by the MinHash signature of their selections within 1,024-row windows
+    K4GroupArgs ga{};
+    ga.sel_idx = sel_idx;
+    ga.sel_cnt = sel_cnt;
+    ga.perm = reinterpret_cast<int32_t*>(w + wl.perm);
+    ga.rows = T;
+    ga.pos0 = q_start;
+    ga.G = p.G;
+    ga.kcap = p.k;
+    k4g_group<<<(unsigned)(p.G * cdiv(T, K4G_WIN)), K4G_THREADS, 0, st>>>(ga);
+    SGQA_CUDA_OK(cudaGetLastError());
+    perm = ga.perm;
+  }
+  if (routed) {
     // each 8-row unit to the kernel that serves it more cheaply (k4r_route.cuh): the
     // warp-level kernel takes its list here, the union kernel below takes the other
     K4RouteArgs ra{};
     ra.sel_idx = sel_idx;
     ra.sel_cnt = sel_cnt;
+    ra.perm = perm;
     ra.choice = reinterpret_cast<int32_t*>(w + wl.choice);
     ra.union_units = reinterpret_cast<int32_t*>(w + wl.union_units);
     ra.warp_units = reinterpret_cast<int32_t*>(w + wl.warp_units);
@@ -454,13 +478,14 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
     a.nsplit = 1;
     a.units = ra.warp_units;
     a.n_units_dev = ra.counts + 1;
+    a.perm = perm;
     a.wait_ns = g_wait_ns;
     CUtensorMap tk, tv;
     if (!make_kv_map(&tk, k, kv_rows) || !make_kv_map(&tv, v, kv_rows)) return SGQA_ERR_CUDA;
     // one CTA of 8 warps per listed unit; CTAs past the list's length return at once
     SGQA_CUDA_OK(launch_k4(a, tk, tv, n_units * 8, true, st));
   }
-  if (kernel == SGQA_ATTN_TC_UNION || kernel == SGQA_ATTN_ROUTED) {
+  if (kernel == SGQA_ATTN_TC_UNION || routed) {
     K4UArgs a{};
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.gate = static_cast<const __nv_bfloat16*>(gate);
@@ -479,6 +504,7 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
     a.wait_ns = g_wait_ns;
     a.units = union_units;
     a.n_units_dev = counts;
+    a.perm = perm;
     CUtensorMap tk, tv;
     if (!make_kv_map(&tk, k, kv_rows) || !make_kv_map(&tv, v, kv_rows)) return SGQA_ERR_CUDA;
     SGQA_CUDA_OK(launch_k4u(a, tk, tv, st));
@@ -802,7 +828,7 @@ sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const void* k, c
   const bool attn_ws_ok = aligned16(ws) && ws_bytes >= attn_ws_layout(p, T).total;
   const int kernel = attn_choice(p, 0, T, q_start, attn_ws_ok);
   if (kernel < 0) return SGQA_ERR_UNSUPPORTED_SHAPE;
-  if (kernel == SGQA_ATTN_ROUTED && !attn_ws_ok) return SGQA_ERR_WORKSPACE_TOO_SMALL;
+  if ((kernel == SGQA_ATTN_ROUTED || kernel == SGQA_ATTN_GROUPED) && !attn_ws_ok) return SGQA_ERR_WORKSPACE_TOO_SMALL;
   s = sgqa_build_block_index(prm, k_proxy, ctx_cap, q_start, q_start + T, k_blk, nb_cap, stream);
   if (s != SGQA_OK) return s;
   s = sgqa_index_topk(prm, q_proxy, T, q_start, k_blk, nb_cap, sel_idx, sel_cnt, ws, ws_bytes, stream);

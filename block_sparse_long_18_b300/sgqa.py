@@ -46,7 +46,7 @@ EXPORTS = (
     "sgqa_status_string", "sgqa_abi_version", "sgqa_index_topk_noalloc", "sgqa_attention_kernel",
     "sgqa_build_block_index_fp8", "sgqa_decode_fp8", "sgqa_prefill_host",
 )
-ATTN_AUTO, ATTN_WARP, ATTN_TC_UNION, ATTN_ROUTED = 0, 1, 2, 3
+ATTN_AUTO, ATTN_WARP, ATTN_TC_UNION, ATTN_ROUTED, ATTN_GROUPED = 0, 1, 2, 3, 4
 
 
 class SgqaError(RuntimeError):
@@ -72,8 +72,8 @@ class Params(ctypes.Structure):
 def params(G=4, Hg=16, D=192, P=256, B=8, k=512, gate_per_dim=1, scale=0.0, attn_kernel=ATTN_AUTO) -> Params:
     """Layer constants; the defaults are the pages' (phantomic12 entry: 64 heads in 4 KV
     groups, head_dim 192, topk 512, proxy_dim 256; ai4snews item: block size 8).
-    attn_kernel: ATTN_AUTO, or ATTN_WARP / ATTN_TC_UNION / ATTN_ROUTED to force a prefill
-    attention kernel."""
+    attn_kernel: ATTN_AUTO, or ATTN_WARP / ATTN_TC_UNION / ATTN_ROUTED / ATTN_GROUPED to force
+    a prefill attention kernel."""
     return Params(G, Hg, D, P, B, k, gate_per_dim, scale, attn_kernel)
 
 
@@ -207,7 +207,7 @@ def sgqa_index_topk_noalloc(prm: Params, q_proxy, q_start: int, k_blk, sel_idx, 
 def sgqa_sparse_attn_fwd(prm: Params, q, k, v, gate, sel_idx, sel_cnt, q_start: int, out, lse=None,
                          dense_mode: bool = False, stream=None, ws=None):
     """ws: optional uint8 workspace of sgqa_workspace_bytes(prm, SGQA_OP_ATTN, T, q_start + T)
-    bytes; it enables the routed mode (the default where the union kernel's shape holds)."""
+    bytes; it enables the grouped mode (the default where the union kernel's shape holds)."""
     T = q.shape[0]
     _check(_lib.sgqa_sparse_attn_fwd(ctypes.byref(prm), _dev(q, BF16, "q"), _dev(k, BF16, "k"), _dev(v, BF16, "v"),
                                      k.shape[1], _dev(gate, BF16, "gate"), _dev(sel_idx, I32, "sel_idx"),

@@ -71,7 +71,7 @@ typedef struct {
   int32_t gate_per_dim;     /* 1: gate is [T, H, D] (element-wise); 0: gate is [T, H] (per head) */
   float softmax_scale;      /* scale on q.k; <= 0 selects 1/sqrt(D) */
   int32_t attn_kernel;      /* prefill attention kernel: SGQA_ATTN_AUTO (0, the default), or
-                               SGQA_ATTN_WARP / _TC_UNION / _ROUTED to force one (see
+                               SGQA_ATTN_WARP / _TC_UNION / _ROUTED / _GROUPED to force one (see
                                sgqa_attention_kernel); other values are INVALID_ARGUMENT */
 } sgqa_params;
 
@@ -83,6 +83,9 @@ typedef struct {
 #define SGQA_ATTN_ROUTED 3    /* each unit of 8 query rows to the union kernel when its union is
                                  small against its rows' selections (they share many blocks),
                                  else to the warp-level kernel (needs the attention workspace) */
+#define SGQA_ATTN_GROUPED 4   /* as SGQA_ATTN_ROUTED, with units of 8 rows drawn from each window of
+                                 4,096 rows in the order of a MinHash signature of their
+                                 selections, so rows that share blocks share units */
 
 /* Operation selector for sgqa_workspace_bytes(). */
 enum { SGQA_OP_INDEX_TOPK = 1, SGQA_OP_PREFILL = 2, SGQA_OP_DECODE = 3, SGQA_OP_ATTN = 4, SGQA_OP_PREFILL_HOST = 5 };
@@ -147,13 +150,13 @@ SGQA_API sgqa_status sgqa_index_topk(const sgqa_params* prm, const void* q_proxy
  *   sel_idx  [G, T, k] int32 ascending, sel_cnt [G, T] int32, read (ignored in dense_mode)
  *   out      [T, H, D] bf16, written;  lse [T, H] fp32, written (may be NULL)
  *   ws       scratch of sgqa_workspace_bytes(prm, SGQA_OP_ATTN, T, q_start + T, 1) bytes
- *            (G * ceil(T/8) * 12 bytes + 256, under 1 MB at T = 131,072), 16-byte aligned, or
- *            NULL / too small: the routed mode (SGQA_ATTN_ROUTED, the default where the union
- *            kernel's shape holds) keeps its per-unit choice and unit lists there; without
+ *            (about G * T * 5.5 bytes: 2.9 MB at T = 131,072), 16-byte aligned, or NULL / too
+ *            small: the grouped mode (SGQA_ATTN_GROUPED, the default where the union kernel's
+ *            shape holds) keeps its row order, per-unit choice and unit lists there; without
  *            it every unit runs on the union kernel.
  * A sel_idx entry outside [0, b_t] sets SGQA_ERR_DEVICE_BOUNDS on the device and the
  * entry is skipped.  Errors: INVALID_ARGUMENT, UNSUPPORTED_SHAPE (a forced kernel outside
- * its shape), WORKSPACE_TOO_SMALL (SGQA_ATTN_ROUTED forced without the workspace).
+ * its shape), WORKSPACE_TOO_SMALL (SGQA_ATTN_ROUTED / _GROUPED forced without the workspace).
  * ------------------------------------------------------------------------------- */
 SGQA_API sgqa_status sgqa_sparse_attn_fwd(const sgqa_params* prm, const void* q, const void* k, const void* v,
                                  int64_t ctx_cap, const void* gate, const int32_t* sel_idx,
@@ -333,12 +336,12 @@ SGQA_API sgqa_status sgqa_selftest_wait_timeout(uint64_t limit_ns, sgqa_stream_t
 
 /* Which attention kernel sgqa_sparse_attn_fwd / sgqa_prefill launch for these arguments
  * given a workspace of sgqa_workspace_bytes(...) bytes (no launch, no device access).  With
- * prm->attn_kernel = SGQA_ATTN_AUTO: SGQA_ATTN_ROUTED whenever the union kernel's shape
+ * prm->attn_kernel = SGQA_ATTN_AUTO: SGQA_ATTN_GROUPED whenever the union kernel's shape
  * holds (blocks of 8, 16 heads per group, top_k_blocks <= 512, every block index of the
  * call below 2^18, i.e. positions below 2,097,152, not dense_mode), SGQA_ATTN_WARP
  * otherwise (an attention call without the workspace runs SGQA_ATTN_TC_UNION instead of
- * the routed mode).  A forced kernel is returned when it can serve the call; a forced union
- * or routed kernel outside its shape returns -1, and the attention entries then fail with
+ * the grouped mode).  A forced kernel is returned when it can serve the call; a forced union,
+ * routed or grouped kernel outside its shape returns -1, and the attention entries then fail with
  * SGQA_ERR_UNSUPPORTED_SHAPE.  Returns -1 for invalid parameters.  Decode always runs the
  * warp-level kernel (split over the context). */
 SGQA_API int32_t sgqa_attention_kernel(const sgqa_params* prm, int64_t T, int64_t q_start, int32_t dense_mode);

@@ -102,24 +102,32 @@ def test_workspace_sizes(lib):
     # 128K prefill: one pass of 8,192 rows x 4 groups x 16,384 fp32 candidates
     ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 131072, 131072)
     assert ws == 4 * 8192 * 16384 * 4
-    # prefill: the indexer's scratch, reused by the routed attention's unit lists
+    # prefill: the indexer's scratch, reused by the grouped attention's row order and unit
+    # lists (4 groups x 131,072 rows x 5.5 bytes)
     wa = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_ATTN, 131072, 131072)
-    assert wa < (1 << 20) and lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL, 131072, 131072) == ws
+    assert wa == 4 * 131072 * 4 + 3 * 4 * 16384 * 4 + 256
+    assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL, 131072, 131072) == ws
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 8) > 0
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 0) == 0
     assert lib.sgqa_workspace_bytes(lib.params(B=3), lib.SGQA_OP_PREFILL, 16, 16) == 0
 
 
 def test_attention_kernel_choice(lib):
-    """Which prefill attention kernel a call launches (no device access): the routed mode
-    (union or warp-level kernel per 8-row unit) wherever the union kernel's shape holds, up
-    to 2M positions; the warp-level kernel for other shapes, dense mode and when forced; -1
+    """Which prefill attention kernel a call launches (no device access): the grouped mode
+    (units of 8 rows with similar selections, each on the union or the warp-level kernel)
+    wherever the union kernel's shape holds, up to 2M positions; the warp-level kernel for other shapes, dense mode and when forced; -1
     for a forced union outside its shape."""
     auto = lib.params()
-    assert lib.sgqa_attention_kernel(auto, 131072, 0) == lib.ATTN_ROUTED
-    assert lib.sgqa_attention_kernel(auto, 8192, 1040384) == lib.ATTN_ROUTED   # the 1M chunk
-    assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8192) == lib.ATTN_ROUTED
-    assert lib.sgqa_attention_kernel(auto, 8192, 2097152 - 8191) == lib.ATTN_WARP  # past 2^18 blocks
+    assert lib.sgqa_attention_kernel(auto, 131072, 0) == lib.ATTN_GROUPED
+    assert lib.sgqa_attention_kernel(auto, 8192, 65536 * 8 - 8192) == lib.ATTN_GROUPED
+    # once every unit's blocks span five or more 16,384-block windows the routing rule sends
+    # no unit to the union kernel (100 * 5 * |union| > 55 * 8 * |union| >= 55 * pairs): the
+    # warp-level kernel alone, without the grouping and routing launches (the 1M chunk)
+    assert lib.sgqa_attention_kernel(auto, 8192, 65536 * 8) == lib.ATTN_WARP
+    assert lib.sgqa_attention_kernel(auto, 8192, 1040384) == lib.ATTN_WARP
+    assert lib.sgqa_attention_kernel(lib.params(attn_kernel=lib.ATTN_GROUPED), 8192, 1040384) == lib.ATTN_GROUPED
+    assert lib.sgqa_attention_kernel(lib.params(attn_kernel=lib.ATTN_TC_UNION), 8192, 2097152 - 8192) == lib.ATTN_TC_UNION
+    assert lib.sgqa_attention_kernel(lib.params(attn_kernel=lib.ATTN_TC_UNION), 8192, 2097152 - 8191) == -1  # past 2^18 blocks
     assert lib.sgqa_attention_kernel(auto, 1024, 0, dense_mode=True) == lib.ATTN_WARP
     assert lib.sgqa_attention_kernel(lib.params(B=4, k=1024), 1024, 0) == lib.ATTN_WARP
     assert lib.sgqa_attention_kernel(lib.params(Hg=8), 1024, 0) == lib.ATTN_WARP
@@ -133,6 +141,9 @@ def test_attention_kernel_choice(lib):
     routed = lib.params(attn_kernel=lib.ATTN_ROUTED)
     assert lib.sgqa_attention_kernel(routed, 131072, 0) == lib.ATTN_ROUTED
     assert lib.sgqa_attention_kernel(lib.params(B=4, k=1024, attn_kernel=lib.ATTN_ROUTED), 1024, 0) == -1
+    grouped = lib.params(attn_kernel=lib.ATTN_GROUPED)
+    assert lib.sgqa_attention_kernel(grouped, 4096, 0) == lib.ATTN_GROUPED
+    assert lib.sgqa_attention_kernel(lib.params(Hg=8, attn_kernel=lib.ATTN_GROUPED), 4096, 0) == -1
     assert lib.sgqa_attention_kernel(lib.params(attn_kernel=7), 1024, 0) == -1
 
 
@@ -142,11 +153,14 @@ def test_forced_union_outside_its_shape_is_rejected(lib):
     f = lib._lib.sgqa_sparse_attn_fwd
     assert f(ctypes.byref(prm), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None, 0, None) == 2
     assert f(ctypes.byref(lib.params(attn_kernel=9)), a, a, a, 4096, a, a, a, 1024, 0, a, None, 0, None, 0, None) == 1
-    # the routed mode forced without its workspace (a choice and two lists per 8-row unit)
+    # the routed and grouped modes forced without their workspace (a choice and two lists per
+    # 8-row unit, the row order)
     routed = lib.params(attn_kernel=lib.ATTN_ROUTED)
     need = lib.sgqa_workspace_bytes(routed, lib.SGQA_OP_ATTN, 1024, 4096)
-    assert need >= 4 * 128 * 12 + 256
+    assert need >= 4 * 128 * 12 + 256 + 4 * 1024 * 4
     assert f(ctypes.byref(routed), a, a, a, 4096, a, a, a, 1024, 3072, a, None, 0, a, need - 256, None) == 3
+    grouped = lib.params(attn_kernel=lib.ATTN_GROUPED)
+    assert f(ctypes.byref(grouped), a, a, a, 4096, a, a, a, 1024, 3072, a, None, 0, None, 0, None) == 3
     # no workspace needed where the union kernel cannot serve
     assert lib.sgqa_workspace_bytes(lib.params(B=4, k=1024), lib.SGQA_OP_ATTN, 1024, 4096) == 256
 

@@ -1,7 +1,7 @@
 """Parity of the union attention kernel (8 query rows per unit over the union of their
-selected blocks, tcgen05 with Q and P in tensor memory), of the warp-level kernel, and of
-the routed mode (each 8-row unit to one of the two by the size of its union) against the
-oracle.  Each is forced through sgqa_params.attn_kernel, and every case first asserts
+selected blocks, tcgen05 with Q and P in tensor memory), of the warp-level kernel, of the
+routed mode (each 8-row unit to one of the two by the size of its union) and of the
+grouped mode (units drawn from 4,096-row windows in MinHash order) against the oracle.  Each is forced through sgqa_params.attn_kernel, and every case first asserts
 through sgqa_attention_kernel that the forced kernel is the one the call launches.  The
 routed mode is also checked bit for bit: every unit's output is the union kernel's or the
 warp-level kernel's, whichever a host restatement of the routing rule picks."""
@@ -87,6 +87,22 @@ def test_routed_attention_sampled_rows_long_context(sg, case):
     _run_case(sg, sg.ATTN_ROUTED, case)
 
 
+@pytest.mark.parametrize("case", UNION_CASES, ids=[f"T{c['T']}_k{c['k']}_q{c.get('q_start', 0)}" for c in UNION_CASES])
+def test_grouped_attention_all_rows(sg, case):
+    _run_case(sg, sg.ATTN_GROUPED, case)
+
+
+@pytest.mark.parametrize("case", UNION_SAMPLED, ids=[f"q{c['q_start']}_T{c['T']}" for c in UNION_SAMPLED])
+def test_grouped_attention_sampled_rows_long_context(sg, case):
+    _run_case(sg, sg.ATTN_GROUPED, case)
+
+
+def test_grouped_attention_ragged_windows_all_rows(sg):
+    """Rows in three 4,096-row grouping windows, the last one ragged, at a position not a
+    multiple of 8: every row against the oracle."""
+    _run_case(sg, sg.ATTN_GROUPED, dict(T=9000, G=2, Hg=16, B=8, k=128, q_start=6003, planted=True))
+
+
 def _route_to_union(sel_idx, sel_cnt, q_start, k):
     """Host restatement of the routing rule: per (group, 8-row unit), the distinct valid
     blocks of its rows' selections (counts clamped to [1, min(k, b_t + 1)], entries outside
@@ -141,9 +157,12 @@ def test_warp_attention_forced(sg, case):
     _run_case(sg, sg.ATTN_WARP, case)
 
 
-def test_auto_choice_is_the_routed_mode_at_1m(sg):
+def test_auto_choice_at_128k_and_1m(sg):
+    """The grouped mode up to where the routing rule can still pick the union kernel; the
+    warp-level kernel alone at the 1M chunk (every unit spans eight windows there)."""
     prm = sg.params()
-    assert sg.sgqa_attention_kernel(prm, 8192, 1040384) == sg.ATTN_ROUTED
+    assert sg.sgqa_attention_kernel(prm, 131072, 0) == sg.ATTN_GROUPED
+    assert sg.sgqa_attention_kernel(prm, 8192, 1040384) == sg.ATTN_WARP
 
 
 def test_union_attention_wait_timeout_is_reported_and_recoverable(sg):
@@ -169,12 +188,12 @@ def test_union_attention_wait_timeout_is_reported_and_recoverable(sg):
     assert torch.equal(out, res.out)
 
 
-def test_routed_attention_wait_timeout_is_reported_and_recoverable(sg):
-    """The routed mode's launches given no time for any bounded wait: the error is
+def test_grouped_attention_wait_timeout_is_reported_and_recoverable(sg):
+    """The grouped mode's launches given no time for any bounded wait: the error is
     reported, nothing hangs, and the next call reproduces the normal output bit for bit."""
     wl = gen.small_workload(T=256, G=2, Hg=16, B=8, k=16, planted=True)
     inp = gen.make_inputs(wl, seed=14, device="cuda")
-    prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k, attn_kernel=sg.ATTN_ROUTED)
+    prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k, attn_kernel=sg.ATTN_GROUPED)
     res = sg.prefill(prm, inp.q, inp.k, inp.v, inp.gate, inp.q_proxy, inp.k_proxy)
     torch.cuda.synchronize()
     assert sg.sgqa_get_device_error() == 0
