@@ -47,6 +47,7 @@ struct K3Args {
   int32_t* pair_idx;    // [G * rows, nseg * (k-1)] their candidate indices (ascending per segment)
   int32_t* pair_cnt;    // [G * rows, nseg] entries each segment kept
   int32_t nseg;         // segments per row
+  int32_t prefetch_ctas;  // a CTA warms L2 for the scores of CTA blockIdx.x + prefetch_ctas (0: off)
   int64_t pos[256];     // decode: absolute position of each row's query
 };
 
@@ -123,6 +124,24 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   const float* row = a.scores + (g * a.rows + i) * a.ld;
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31, warp = tid >> 5;
+  // Warm L2 for the scores of the CTA about two waves later (launched when a CTA of this
+  // wave retires), one 128-byte line per thread, so that its row load hits L2.
+  if (MODE != K3_MERGE && !STREAM && a.prefetch_ctas > 0) {
+    const int64_t cb = (int64_t)blockIdx.x + a.prefetch_ctas;
+    const int64_t nseg2 = MODE == K3_SEGMENT ? a.nseg : 1;
+    if (cb < (int64_t)a.G * a.rows * nseg2) {
+      const int64_t r2 = cb / nseg2, seg2 = cb % nseg2;
+      const int64_t i2 = r2 % a.rows;
+      const int64_t bt2 = (a.use_pos ? a.pos[i2] : a.pos0 + i2) / a.B;
+      const int64_t b2 = MODE == K3_SEGMENT ? seg2 * (NT * PER) : 0;
+      int64_t n2 = bt2 - b2;
+      n2 = n2 < (int64_t)NT * PER ? n2 : (int64_t)NT * PER;
+      if ((int64_t)tid * 32 < n2) {
+        const float* p2 = a.scores + ((r2 / a.rows) * a.rows + i2) * a.ld + b2 + (int64_t)tid * 32;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p2));
+      }
+    }
+  }
   // n: candidate slots of this CTA; base: candidate index of slot 0 (K3_SEGMENT)
   int64_t n = bt, base = 0;
   if (MODE == K3_SEGMENT) {

@@ -237,9 +237,18 @@ void launch_k3_regs(const K3Args& a, int64_t max_cand, int64_t grid, cudaStream_
 // One CTA per row; the block is the smallest whose registers (up to 32 keys per thread)
 // hold the launch's longest row.  Longer rows go through the segment + merge pair when
 // `wsl` gives them pair buffers inside `ws`.
+#ifndef SGQA_K3_PREFETCH_WAVES
+#define SGQA_K3_PREFETCH_WAVES 1
+#endif
 cudaError_t launch_k3(K3Args a, int64_t max_cand, uint8_t* ws, const IndexWs& wsl, cudaStream_t st) {
   const int64_t grid = (int64_t)a.G * a.rows;
   if (grid <= 0) return cudaSuccess;
+  // prefetch distance: resident CTAs (1,024 threads per SM) times the waves ahead (one
+  // wave measured best on B300: 128K indexer + top-k 16.97 -> 16.46 ms; two 16.50, four 17.50)
+  {
+    const int nt = max_cand <= 128 * kK3Per ? 128 : (max_cand <= 256 * kK3Per ? 256 : kK3Threads);
+    a.prefetch_ctas = SGQA_K3_PREFETCH_WAVES * num_sms() * (1024 / nt);
+  }
   if (max_cand <= 128 * kK3Per) {
     launch_k3_regs<128>(a, max_cand, grid, st);
   } else if (max_cand <= 256 * kK3Per) {

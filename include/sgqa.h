@@ -189,7 +189,10 @@ SGQA_API sgqa_status sgqa_prefill(const sgqa_params* prm, const void* q, const v
  * (causality), so its copy-in, its prefill (a chunked prefill at q_start + its first row)
  * and its copy-out run on three streams and overlap with the neighbouring chunks: the
  * library copies in on one stream of its own, computes on `stream` and copies out on a
- * second stream of its own.  Outputs are bit-identical to one sgqa_prefill over all rows.
+ * second stream of its own.  Selections are identical to one sgqa_prefill over all rows,
+ * and so are outputs and LSE when chunk_rows is a multiple of 4,096 (the grouped attention
+ * mode's window, which then forms the same units); other chunk sizes change only the fp32
+ * summation order of the attention.
  *
  * Host tensors (pinned memory for overlapped copies; pageable memory works but the
  * copies then serialise with the host):

@@ -228,13 +228,14 @@ def test_small_workspace_many_passes(sg):
 def test_host_prefill_pipeline_equals_device_prefill(sg, q_start, gate_per_dim):
     """The end-to-end entry sgqa_prefill_host (pinned host tensors, chunks of rows
     pipelined by the library over its copy-in stream, the calling stream and its copy-out
-    stream) gives bit-identical outputs and LSE to one prefill call on device tensors."""
-    wl = gen.small_workload(T=2600, G=2, Hg=16, B=8, k=24, planted=True, q_start=q_start)
+    stream) gives bit-identical outputs, LSE and block index to one prefill call on device
+    tensors when its chunks are whole grouping windows (4,096 rows)."""
+    wl = gen.small_workload(T=9000, G=2, Hg=16, B=8, k=24, planted=True, q_start=q_start)
     inp = _to_cuda(gen.make_inputs(wl, seed=11))
     prm = _prm(sg, wl, gate_per_dim=gate_per_dim)
     gate = inp.gate if gate_per_dim else inp.gate[:, :, 0].contiguous()
     res = _gpu_prefill(sg, inp, wl, prm, gate=gate)
-    hp = sg.HostPrefill(prm, wl.T, wl.C, wl.q_start, chunk_rows=1024, with_lse=True)  # three chunks
+    hp = sg.HostPrefill(prm, wl.T, wl.C, wl.q_start, chunk_rows=4096, with_lse=True)  # three chunks
     host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "q_proxy", "k_proxy")}
     host["gate"] = gate.cpu().pin_memory()
     for _ in range(2):  # a second run reuses every buffer
@@ -245,6 +246,25 @@ def test_host_prefill_pipeline_equals_device_prefill(sg, q_start, gate_per_dim):
         assert torch.equal(out, res.out.cpu())
         assert torch.equal(hp.lse_host, res.lse.cpu())
         assert torch.equal(hp.d["k_blk"], res.k_blk)
+
+
+def test_host_prefill_small_chunks_within_tolerance(sg):
+    """Chunks of 1,024 rows (smaller than a grouping window): the attention's units differ
+    from one call over all rows, so outputs agree within the attention tolerance and LSE
+    within its bound; the block index is identical."""
+    wl = gen.small_workload(T=2600, G=2, Hg=16, B=8, k=24, planted=True, q_start=1000)
+    inp = _to_cuda(gen.make_inputs(wl, seed=11))
+    prm = _prm(sg, wl)
+    res = _gpu_prefill(sg, inp, wl, prm)
+    hp = sg.HostPrefill(prm, wl.T, wl.C, wl.q_start, chunk_rows=1024, with_lse=True)
+    host = {n: getattr(inp, n).cpu().pin_memory() for n in ("q", "k", "v", "gate", "q_proxy", "k_proxy")}
+    out = hp.run(host)
+    torch.cuda.synchronize()
+    assert sg.sgqa_get_device_error() == 0
+    assert torch.equal(hp.d["k_blk"], res.k_blk)
+    d = (out.float() - res.out.cpu().float()).abs()
+    assert float(d.max()) <= 2e-2 and float(d.mean()) <= 1e-3, (float(d.max()), float(d.mean()))
+    assert float((hp.lse_host - res.lse.cpu()).abs().max()) <= LSE_ABS
 
 
 def test_block_index_real_valued_proxies_within_one_ulp(sg):
