@@ -38,7 +38,7 @@ METRIC = "Sparse GQA prefill tokens/s per layer @128K (1×B300); % of roofline p
 HBM_FALLBACK_GBS, BF16_FALLBACK_TFS = 6400.0, 1800.0
 
 K4_KERNEL = {1: "k4_sparse_attn", 2: "k4u_sparse_attn", 3: "k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn",
-             4: "k4g_group + k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn"}
+             4: "k4g_signature + k4g_sort + k4r_count + k4r_compact + k4_sparse_attn + k4u_sparse_attn"}
 
 
 def load_peaks():
@@ -85,31 +85,25 @@ def work_model(wl):
 _I64_MIN = -(1 << 63)
 
 
-def _lsr(x, s):
-    """Logical right shift of int64 tensors holding 64-bit patterns."""
-    return (x >> s) & ((1 << (64 - s)) - 1)
-
-
-def _splitmix(x):
-    """The splitmix64 output function on int64 tensors (wrap-around arithmetic), as the
-    library's grouping kernel applies it."""
-    c1 = 0xbf58476d1ce4e5b9 - (1 << 64)
-    c2 = 0x94d049bb133111eb - (1 << 64)
-    x = x ^ _lsr(x, 30)
-    x = x * c1
-    x = x ^ _lsr(x, 27)
-    x = x * c2
-    return x ^ _lsr(x, 31)
-
-
 GROUP_WINDOW = 4096  # rows per grouping window of the library's grouped attention mode
+
+
+def _murmur32(x):
+    """The 32-bit MurmurHash3 finalizer on int64 tensors holding 32-bit words, as the
+    library's grouping kernel applies it."""
+    m = 0xFFFFFFFF
+    x = x ^ (x >> 16)
+    x = (x * 0x85ebca6b) & m
+    x = x ^ (x >> 13)
+    x = (x * 0xc2b2ae35) & m
+    return x ^ (x >> 16)
 
 
 def grouped_row_order(sel, cnt, wl, win=GROUP_WINDOW):
     """The grouped attention mode's row order, restated with torch for the benchmark's
-    routing statistics: per group and window of `win` rows, the rows sorted by (high 32 bits
-    of the least splitmix64 hash of their selected blocks, 22 bits of a second such hash,
-    row).  Returns perm [G, T] (the row at each slot)."""
+    routing statistics: per group and window of `win` rows, the rows sorted by (the least
+    32-bit hash of their selected blocks, high bits of a second such hash, row).  Returns
+    perm [G, T] (the row at each slot)."""
     G, T, k = sel.shape
     dev = sel.device
     perm = torch.empty((G, T), dtype=torch.int64, device=dev)
@@ -117,19 +111,20 @@ def grouped_row_order(sel, cnt, wl, win=GROUP_WINDOW):
     bt = (wl.q_start + i) // wl.B
     cap = torch.clamp(bt + 1, max=k)
     j = torch.arange(k, device=dev)
+    row_bits = win.bit_length() - 1
     for g in range(G):
         c = cnt[g].long()
         c = torch.where(c < 1, torch.ones_like(c), torch.minimum(c, cap))
         b = sel[g].long()
         valid = (j[None, :] < c[:, None]) & (b >= 0) & (b <= bt[:, None])
-        big = torch.full_like(b, (1 << 63) - 1)
-        h1 = torch.where(valid, _splitmix(b) ^ _I64_MIN, big).amin(dim=1) ^ _I64_MIN
-        h2 = torch.where(valid, _splitmix(b ^ 0x5bd1e9955bd1e995) ^ _I64_MIN, big).amin(dim=1) ^ _I64_MIN
-        row_bits = win.bit_length() - 1
-        key = (h1 & -(1 << 32)) | (_lsr(h2, 32 + row_bits) << row_bits) | (i % win)
+        big = torch.full_like(b, 1 << 32)
+        h1 = torch.where(valid, _murmur32(b & 0xFFFFFFFF), big).amin(dim=1).clamp(max=0xFFFFFFFF)
+        h2 = torch.where(valid, _murmur32((b & 0xFFFFFFFF) ^ 0x5bd1e995), big).amin(dim=1).clamp(max=0xFFFFFFFF)
+        # (h1 << 32 | ...) compared as unsigned: flip the sign bit for torch's signed sort
+        key = ((h1 << 32) | ((h2 >> row_bits) << row_bits) | (i % win)) ^ _I64_MIN
         nwin = (T + win - 1) // win
         pad = nwin * win - T
-        keyw = torch.cat([key ^ _I64_MIN, torch.full((pad,), (1 << 63) - 1, device=dev, dtype=torch.int64)])
+        keyw = torch.cat([key, torch.full((pad,), (1 << 63) - 1, device=dev, dtype=torch.int64)])
         srt, _ = torch.sort(keyw.view(nwin, win), dim=1)
         order = ((srt ^ _I64_MIN) & (win - 1)) + torch.arange(nwin, device=dev)[:, None] * win
         perm[g] = order.reshape(-1)[:T]
@@ -571,9 +566,9 @@ def run_sgqa(args, rank, world, local_rank):
     # K1 once, K2 + top-k per 8,192-row pass (top-k in two launches for rows past 16,384
     # candidates: per-slice selection, then the merge), K4 once
     # (the routed attention: two routing launches and the warp-level kernel besides the union
-    # one; the grouped mode one more for the row order)
+    # one; the grouped mode two more for the row order)
     kind = sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start)
-    launches_per_step = 2 + {sgqa.ATTN_ROUTED: 3, sgqa.ATTN_GROUPED: 4}.get(kind, 0)
+    launches_per_step = 2 + {sgqa.ATTN_ROUTED: 3, sgqa.ATTN_GROUPED: 5}.get(kind, 0)
     for r0 in range(0, wl.T, 8192):
         cand_last = (wl.q_start + min(wl.T, r0 + 8192) - 1) // wl.B
         launches_per_step += (1 if cand_last > 0 else 0) + (2 if cand_last > 16384 and wl.k > 1 else 1)

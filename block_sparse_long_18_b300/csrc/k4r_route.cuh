@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(K4R_COMPACT_THREADS) k4r_compact(const K4Route
 
 
 // ---------------------------------------------------------------------------------------
-// Grouped units: one CTA of K4G_THREADS threads per (group, window of K4G_WIN rows).
+// Grouped units: k4g_signature (a warp per row) writes each row's sort key; k4g_sort (a CTA
+// per (group, window of K4G_WIN rows)) orders the window.
 // ---------------------------------------------------------------------------------------
 #ifndef SGQA_GROUP_WINDOW
 #define SGQA_GROUP_WINDOW 4096
@@ -155,65 +156,72 @@ constexpr int K4G_WIN = SGQA_GROUP_WINDOW;   // rows per grouping window (a powe
 constexpr int K4G_THREADS = 1024;
 static_assert(K4G_WIN >= K4G_THREADS && (K4G_WIN & (K4G_WIN - 1)) == 0, "grouping window");
 
-// The splitmix64 output function (Steele, Lea and Flood, "Fast splittable pseudorandom
-// number generators", 2014): a bijective 64-bit mixer.
-__device__ __forceinline__ uint64_t k4g_mix(uint64_t x) {
-  x ^= x >> 30;
-  x *= 0xbf58476d1ce4e5b9ull;
-  x ^= x >> 27;
-  x *= 0x94d049bb133111ebull;
-  x ^= x >> 31;
-  return x;
+// The 32-bit finalizer of MurmurHash3 (Austin Appleby, public domain): a bijective mixer
+// of a 32-bit word.  The two signatures hash the block index and the block index xor a
+// constant.
+__device__ __forceinline__ uint32_t k4g_mix(uint32_t h) {
+  h ^= h >> 16;
+  h *= 0x85ebca6bu;
+  h ^= h >> 13;
+  h *= 0xc2b2ae35u;
+  h ^= h >> 16;
+  return h;
 }
+constexpr uint32_t K4G_SEED2 = 0x5bd1e995u;
 
 struct K4GroupArgs {
   const int32_t* sel_idx;  // [G, rows, kcap]
   const int32_t* sel_cnt;  // [G, rows]
+  uint64_t* keys;          // [G, rows] sort keys (k4g_signature), read by k4g_sort
   int32_t* perm;           // [G, rows]
   int64_t rows, pos0;
   int32_t G, kcap;
 };
+constexpr int K4G_SIG_WARPS = 8;
 
-__global__ void __launch_bounds__(K4G_THREADS) k4g_group(const K4GroupArgs a) {
+// Sort key of every row, one warp per row: the least first hash over the row's valid
+// selected blocks, then the high bits of the least second hash, then the row's place in its
+// window.  The same entry rules as the union builder.
+__global__ void __launch_bounds__(K4G_SIG_WARPS * 32) k4g_signature(const K4GroupArgs a) {
+  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
+  const int64_t r = (int64_t)blockIdx.x * K4G_SIG_WARPS + warp;  // (group, row)
+  if (r >= (int64_t)a.G * a.rows) return;
+  const int64_t g = r / a.rows, i = r % a.rows;
+  const int32_t bt = (int32_t)((a.pos0 + i) >> 3);
+  int32_t c = __ldg(a.sel_cnt + r);
+  const int32_t cap = a.kcap < bt + 1 ? a.kcap : bt + 1;
+  if (c < 1 || c > cap) c = c < 1 ? 1 : cap;
+  const int32_t* sel = a.sel_idx + r * a.kcap;
+  uint32_t h1 = ~0u, h2 = ~0u;
+  for (int32_t j = (int32_t)lane; j < c; j += 32) {
+    const int32_t b = __ldg(sel + j);
+    if (b < 0 || b > bt) continue;
+    h1 = min(h1, k4g_mix((uint32_t)b));
+    h2 = min(h2, k4g_mix((uint32_t)b ^ K4G_SEED2));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    h1 = min(h1, __shfl_xor_sync(0xffffffffu, h1, o));
+    h2 = min(h2, __shfl_xor_sync(0xffffffffu, h2, o));
+  }
+  constexpr int kRowBits = __builtin_ctz(K4G_WIN);
+  if (lane == 0)
+    a.keys[r] = ((uint64_t)h1 << 32) | ((uint64_t)(h2 >> kRowBits) << kRowBits) | (uint64_t)(i & (K4G_WIN - 1));
+  (void)g;
+}
+
+// One CTA per (group, window): bitonic sort of the window's keys in shared memory; the
+// sorted keys' low bits give the row order.
+__global__ void __launch_bounds__(K4G_THREADS) k4g_sort(const K4GroupArgs a) {
   __shared__ uint64_t key[K4G_WIN];
   const int64_t nwin = (a.rows + K4G_WIN - 1) / K4G_WIN;
   const int32_t g = (int32_t)(blockIdx.x / nwin);
   const int64_t w0 = (int64_t)(blockIdx.x % nwin) * K4G_WIN;
   const int nrow = (int)(a.rows - w0 < K4G_WIN ? a.rows - w0 : K4G_WIN);
-  const uint32_t warp = threadIdx.x >> 5, lane = lane_id();
-  // signature of row w0 + r, one warp per row; the same entry rules as the union builder
-  for (int r = (int)warp; r < K4G_WIN; r += K4G_THREADS / 32) {
-    uint64_t h1 = ~0ull, h2 = ~0ull;
-    if (r < nrow) {
-      const int64_t i = w0 + r;
-      const int32_t bt = (int32_t)((a.pos0 + i) >> 3);
-      int32_t c = __ldg(a.sel_cnt + (int64_t)g * a.rows + i);
-      const int32_t cap = a.kcap < bt + 1 ? a.kcap : bt + 1;
-      if (c < 1 || c > cap) c = c < 1 ? 1 : cap;
-      const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + i) * a.kcap;
-      for (int32_t j = (int32_t)lane; j < c; j += 32) {
-        const int32_t b = __ldg(sel + j);
-        if (b < 0 || b > bt) continue;
-        const uint64_t x = k4g_mix((uint64_t)(uint32_t)b);
-        h1 = x < h1 ? x : h1;
-        const uint64_t y = k4g_mix((uint64_t)(uint32_t)b ^ 0x5bd1e9955bd1e995ull);
-        h2 = y < h2 ? y : h2;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const uint64_t x = __shfl_xor_sync(0xffffffffu, h1, o), y = __shfl_xor_sync(0xffffffffu, h2, o);
-        h1 = x < h1 ? x : h1;
-        h2 = y < h2 ? y : h2;
-      }
-    }
-    // sort key: high 32 bits of the first hash, then bits of the second, then the row
-    constexpr int kRowBits = __builtin_ctz(K4G_WIN);
-    if (lane == 0)
-      key[r] = r < nrow ? ((h1 & 0xFFFFFFFF00000000ull) | ((h2 >> (32 + kRowBits)) << kRowBits) | (uint64_t)r)
-                        : ~0ull;
-  }
+  for (int t = threadIdx.x; t < K4G_WIN; t += K4G_THREADS)
+    key[t] = t < nrow ? a.keys[(int64_t)g * a.rows + w0 + t] : ~0ull;
   __syncthreads();
-  // bitonic sort of the window's keys, ascending (thread t owns elements t, t + 1024, ...)
+  // ascending; thread t owns elements t, t + 1024, ...
   for (uint32_t k = 2; k <= (uint32_t)K4G_WIN; k <<= 1) {
     for (uint32_t j = k >> 1; j > 0; j >>= 1) {
       for (uint32_t t = threadIdx.x; t < (uint32_t)K4G_WIN; t += K4G_THREADS) {

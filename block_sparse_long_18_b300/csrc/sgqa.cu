@@ -389,9 +389,9 @@ int attn_choice(const Prm& p, int32_t dense, int64_t T, int64_t q_start, bool ws
 
 // Workspace of the routed and grouped attention modes for T query rows: the per-unit
 // choice, the two unit lists and their lengths (units = G x ceil(T / 8)), and the grouped
-// mode's row order [G, T].
+// mode's row order [G, T] and sort keys [G, T].
 struct AttnWs {
-  size_t choice, union_units, warp_units, counts, perm, total;
+  size_t choice, union_units, warp_units, counts, perm, keys, total;
 };
 AttnWs attn_ws_layout(const Prm& p, int64_t T) {
   AttnWs w{};
@@ -401,7 +401,8 @@ AttnWs attn_ws_layout(const Prm& p, int64_t T) {
   w.warp_units = w.union_units + align_up(nu * 4, 256);
   w.counts = w.warp_units + align_up(nu * 4, 256);
   w.perm = w.counts + 256;
-  w.total = w.perm + align_up((size_t)p.G * (size_t)std::max<int64_t>(T, 0) * 4, 256);
+  w.keys = w.perm + align_up((size_t)p.G * (size_t)std::max<int64_t>(T, 0) * 4, 256);
+  w.total = w.keys + align_up((size_t)p.G * (size_t)std::max<int64_t>(T, 0) * 8, 256);
   return w;
 }
 
@@ -435,11 +436,14 @@ sgqa_status run_attention(const Prm& p, const void* q, const void* k, const void
     ga.sel_idx = sel_idx;
     ga.sel_cnt = sel_cnt;
     ga.perm = reinterpret_cast<int32_t*>(w + wl.perm);
+    ga.keys = reinterpret_cast<uint64_t*>(w + wl.keys);
     ga.rows = T;
     ga.pos0 = q_start;
     ga.G = p.G;
     ga.kcap = p.k;
-    k4g_group<<<(unsigned)(p.G * cdiv(T, K4G_WIN)), K4G_THREADS, 0, st>>>(ga);
+    k4g_signature<<<(unsigned)cdiv((int64_t)p.G * T, K4G_SIG_WARPS), K4G_SIG_WARPS * 32, 0, st>>>(ga);
+    SGQA_CUDA_OK(cudaGetLastError());
+    k4g_sort<<<(unsigned)(p.G * cdiv(T, K4G_WIN)), K4G_THREADS, 0, st>>>(ga);
     SGQA_CUDA_OK(cudaGetLastError());
     perm = ga.perm;
   }

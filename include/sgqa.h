@@ -150,7 +150,7 @@ SGQA_API sgqa_status sgqa_index_topk(const sgqa_params* prm, const void* q_proxy
  *   sel_idx  [G, T, k] int32 ascending, sel_cnt [G, T] int32, read (ignored in dense_mode)
  *   out      [T, H, D] bf16, written;  lse [T, H] fp32, written (may be NULL)
  *   ws       scratch of sgqa_workspace_bytes(prm, SGQA_OP_ATTN, T, q_start + T, 1) bytes
- *            (about G * T * 5.5 bytes: 2.9 MB at T = 131,072), 16-byte aligned, or NULL / too
+ *            (about G * T * 13.5 bytes: 7.1 MB at T = 131,072), 16-byte aligned, or NULL / too
  *            small: the grouped mode (SGQA_ATTN_GROUPED, the default where the union kernel's
  *            shape holds) keeps its row order, per-unit choice and unit lists there; without
  *            it every unit runs on the union kernel.

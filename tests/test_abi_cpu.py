@@ -102,10 +102,10 @@ def test_workspace_sizes(lib):
     # 128K prefill: one pass of 8,192 rows x 4 groups x 16,384 fp32 candidates
     ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 131072, 131072)
     assert ws == 4 * 8192 * 16384 * 4
-    # prefill: the indexer's scratch, reused by the grouped attention's row order and unit
-    # lists (4 groups x 131,072 rows x 5.5 bytes)
+    # prefill: the indexer's scratch, reused by the grouped attention's sort keys, row order
+    # and unit lists (4 groups x 131,072 rows x 13.5 bytes)
     wa = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_ATTN, 131072, 131072)
-    assert wa == 4 * 131072 * 4 + 3 * 4 * 16384 * 4 + 256
+    assert wa == 4 * 131072 * (8 + 4) + 3 * 4 * 16384 * 4 + 256
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_PREFILL, 131072, 131072) == ws
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 8) > 0
     assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_DECODE, 1, 1 << 20, 0) == 0
@@ -157,7 +157,7 @@ def test_forced_union_outside_its_shape_is_rejected(lib):
     # 8-row unit, the row order)
     routed = lib.params(attn_kernel=lib.ATTN_ROUTED)
     need = lib.sgqa_workspace_bytes(routed, lib.SGQA_OP_ATTN, 1024, 4096)
-    assert need >= 4 * 128 * 12 + 256 + 4 * 1024 * 4
+    assert need >= 4 * 128 * 12 + 256 + 4 * 1024 * 12
     assert f(ctypes.byref(routed), a, a, a, 4096, a, a, a, 1024, 3072, a, None, 0, a, need - 256, None) == 3
     grouped = lib.params(attn_kernel=lib.ATTN_GROUPED)
     assert f(ctypes.byref(grouped), a, a, a, 4096, a, a, a, 1024, 3072, a, None, 0, None, 0, None) == 3
