@@ -427,7 +427,10 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
     const uint32_t tS16 = tmem + lb16 + K4U_COL_S, tP16 = tmem + lb16 + K4U_COL_P, tO16 = tmem + lb16 + K4U_COL_O;
     float* xchg = reinterpret_cast<float*>(smem + K4U_X_OFF);  // row sums per pair, for the epilogue
     const float sl2 = a.scale_log2;
-    constexpr float kLazy = 8.f;  // reference maximum refreshed only past 2^8
+    // A lane's chunk sum of P past 2^16 (a reference maximum unset or far too low) sends the
+    // chunk through the rescale; below it every P stays under 2^16, where bf16 P and the fp32
+    // sums keep their relative precision
+    constexpr float kLazySum = 65536.f;
 
     auto write_q = [&](int64_t u) {  // this half of the Q rows of unit u -> tensor memory
       const int64_t uid = unit_id(u);
@@ -541,36 +544,37 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
             for (int e = 0; e < 4; ++e)
               if (k == ownj && (int32_t)(kq + (e & 1)) > tlim_r) s[4 * k + e] = -INFINITY;
         }
-        // P = 2^(scale_log2 * s - m) on the row's blocks with the current references; the
-        // first pass also finds the chunk's maxima, and a reference more than 2^8 too low
-        // sends the chunk through a second pass after the rescale
+        // P = 2^(scale_log2 * s - m) on the row's blocks with the current references, with no
+        // branch: a block the row did not select gets the exponent offset -inf, so its P is 0.
+        // A lane sum past kLazySum (some P far above 1) sends the chunk through a second pass
+        // after the rescale to the chunk's true maxima.
         uint32_t pw[32];
-        float lca = 0.f, lcb = 0.f, xa = -INFINITY, xb = -INFINITY;
-        auto ppass = [&](bool track) {
+        float lca = 0.f, lcb = 0.f;
+        auto ppass = [&]() {
           lca = 0.f;
           lcb = 0.f;
+          const float na = -ma, nb = -mb;
 #pragma unroll
           for (int k = 0; k < K4U_CB; ++k) {
-            uint32_t w0 = 0u, w1 = 0u;
-            if ((mine >> k) & 1u) {
-              const float x0 = s[4 * k], x1 = s[4 * k + 1], x2 = s[4 * k + 2], x3 = s[4 * k + 3];
-              if (track) {
-                xa = fmaxf(xa, fmaxf(x0, x1));
-                xb = fmaxf(xb, fmaxf(x2, x3));
-              }
-              const float p0 = fast_exp2(fmaf(x0, sl2, -ma)), p1 = fast_exp2(fmaf(x1, sl2, -ma));
-              const float p2 = fast_exp2(fmaf(x2, sl2, -mb)), p3 = fast_exp2(fmaf(x3, sl2, -mb));
-              lca += p0 + p1;
-              lcb += p2 + p3;
-              w0 = pack_bf16(p0, p1);
-              w1 = pack_bf16(p2, p3);
-            }
-            pw[2 * k] = w0;
-            pw[2 * k + 1] = w1;
+            const bool mk = ((mine >> k) & 1u) != 0u;
+            const float ca = mk ? na : -INFINITY, cb = mk ? nb : -INFINITY;
+            const float p0 = fast_exp2(fmaf(s[4 * k], sl2, ca)), p1 = fast_exp2(fmaf(s[4 * k + 1], sl2, ca));
+            const float p2 = fast_exp2(fmaf(s[4 * k + 2], sl2, cb)), p3 = fast_exp2(fmaf(s[4 * k + 3], sl2, cb));
+            lca += p0 + p1;
+            lcb += p2 + p3;
+            pw[2 * k] = pack_bf16(p0, p1);
+            pw[2 * k + 1] = pack_bf16(p2, p3);
           }
         };
-        ppass(true);
-        if (__any_sync(0xffffffffu, xa * sl2 > ma + kLazy || xb * sl2 > mb + kLazy)) {
+        ppass();
+        if (__any_sync(0xffffffffu, !(lca <= kLazySum) || !(lcb <= kLazySum))) {
+          float xa = -INFINITY, xb = -INFINITY;
+#pragma unroll
+          for (int k = 0; k < K4U_CB; ++k)
+            if ((mine >> k) & 1u) {
+              xa = fmaxf(xa, fmaxf(s[4 * k], s[4 * k + 1]));
+              xb = fmaxf(xb, fmaxf(s[4 * k + 2], s[4 * k + 3]));
+            }
 #pragma unroll
           for (int o = 1; o <= 2; o <<= 1) {
             xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, o));
@@ -598,7 +602,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
             }
             tmem_st_wait();
           }
-          ppass(false);
+          ppass();
         }
         la += lca;
         lb += lcb;
@@ -674,8 +678,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
               g0 = f.x;
               g1 = f.y;
             }
-            const float s0v = __frcp_rn(1.f + fast_exp2(-g0 * kLog2e));
-            const float s1v = __frcp_rn(1.f + fast_exp2(-g1 * kLog2e));
+            const float s0v = fast_rcp(1.f + fast_exp2(-g0 * kLog2e));
+            const float s1v = fast_rcp(1.f + fast_exp2(-g1 * kLog2e));
             y[e] = pack_bf16(__uint_as_float(o[2 * e]) * inv * s0v, __uint_as_float(o[2 * e + 1]) * inv * s1v);
           }
           uint4* dst = reinterpret_cast<uint4*>(a.out + hb * K4U_D + 96 * hf + 32 * cc);

@@ -390,6 +390,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// Reciprocal to about one ulp (rcp.approx); the gate's sigmoid ends in bf16, where that
+// error does not show.
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------------------------------------------------
 // cp.async (16-byte, L2 only)
 // ------------------------------------------------------------------------------------
