@@ -94,8 +94,12 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
   const uint32_t sb0 = smem_u32(smem);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + K4U_BAR_OFF);
   auto bar = [&](int idx) { return smem_u32(&bars[idx]); };
-  enum { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kTblFull = 8, kTblEmpty = 10, kSFull = 12, kSFree = 13,
-         kPFull = 14, kPvDone = 15, kQFull = 16, kQEmpty = 17, kOEmpty = 18, kFinal = 19 };
+  // kKEmpty + s completes when S of the chunk in K slot s is done (the slot and the S columns
+  // may be reused, the chunk's scores read; after a unit's last chunk, Q too); kVEmpty + s
+  // when O += P V of the chunk in V slot s is done (the slot and the P columns free).  A
+  // waiter is never two phases behind on either, so the parity of its chunk identifies it.
+  enum { kKFull = 0, kKEmpty = 2, kVFull = 4, kVEmpty = 6, kTblFull = 8, kTblEmpty = 10, kSFree = 12, kPFull = 13,
+         kQFull = 14, kOEmpty = 15, kFinal = 16 };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + K4U_BAR_OFF + 256);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + K4U_BAR_OFF + 260);
 
@@ -120,12 +124,9 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       mbar_init(bar(kTblFull + s), 1);
       mbar_init(bar(kTblEmpty + s), 11);  // K and V producers, MMA thread, 8 softmax warps
     }
-    mbar_init(bar(kSFull), 1);
     mbar_init(bar(kSFree), 8);
     mbar_init(bar(kPFull), 8);
-    mbar_init(bar(kPvDone), 1);
     mbar_init(bar(kQFull), 8);
-    mbar_init(bar(kQEmpty), 1);
     mbar_init(bar(kOEmpty), 8);
     mbar_init(bar(kFinal), 1);
     *abort_flag = 0;
@@ -349,14 +350,24 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         }
   } else if (warp == 1) {
     // ------------------------------- MMA issuer -------------------------------
+    // A tcgen05.mma issue takes as long as the MMA runs (about 65 cycles at N = 128), so the
+    // tensor pipe idles whenever this thread is not issuing: one commit per product, and the
+    // inputs of each O are tested (without blocking) before the S ahead of it is issued.
     if (lane == 0) {
       const uint32_t id_s = idesc_bf16_f32(128, 128);
       const uint32_t id_o = idesc_bf16_f32(128, 192) | (1u << 16);  // B (V) is MN-major
       uint32_t uc = 0, kc = 0;
       bool ok = true;
-      auto issue_o = [&](uint32_t c, bool first) -> bool {
-        if (!mbar_wait(bar(kPFull), c & 1, a.wait_ns, abort_flag, kSuspendNs)) return false;
-        if (!mbar_wait(bar(kVFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) return false;
+      auto issue_s = [&](uint32_t c) {
+        tc_fence_after();
+        const uint32_t kb = sb0 + K4U_K_OFF + (c & 1) * K4U_SLOT;
+#pragma unroll
+        for (int ks = 0; ks < 12; ++ks)
+          tc_mma_ts(tmem + K4U_COL_S, tmem + K4U_COL_Q + 8 * ks,
+                    smem_desc_k_sw128_sbo(kb + (ks >> 2) * 1024 + (ks & 3) * 32, 3072), id_s, ks > 0 ? 1u : 0u);
+        tc_commit(bar(kKEmpty + (c & 1)));
+      };
+      auto issue_o = [&](uint32_t c, bool first) {
         tc_fence_after();
         const uint32_t vb = sb0 + K4U_V_OFF + (c & 1) * K4U_SLOT;
 #pragma unroll
@@ -364,8 +375,18 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
           tc_mma_ts(tmem + K4U_COL_O, tmem + K4U_COL_P + 8 * ks, smem_desc_mn_sw128(vb + ks * 6144, 1024, 3072),
                     id_o, (first && ks == 0) ? 0u : 1u);
         tc_commit(bar(kVEmpty + (c & 1)));
-        tc_commit(bar(kPvDone));
-        return true;
+      };
+      auto s_wait = [&](uint32_t c) -> bool {
+        return mbar_wait(bar(kKFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs) &&
+               (c == 0 || mbar_wait(bar(kSFree), (c - 1) & 1, a.wait_ns, abort_flag, kSuspendNs));
+      };
+      // inputs of O(c): P(c), V(c)
+      auto o_ready = [&](uint32_t c) -> bool {
+        return mbar_test_wait(bar(kPFull), c & 1) & mbar_test_wait(bar(kVFull + (c & 1)), (c >> 1) & 1);
+      };
+      auto o_wait = [&](uint32_t c) -> bool {
+        return mbar_wait(bar(kPFull), c & 1, a.wait_ns, abort_flag, kSuspendNs) &&
+               mbar_wait(bar(kVFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs);
       };
       for (int64_t u = blockIdx.x; u < n_units && ok; u += gridDim.x, ++uc) {
         const uint32_t buf = uc & 1;
@@ -373,34 +394,30 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         const int32_t nU = reinterpret_cast<const int32_t*>(tbl(buf) + K4U_TB_META)[0];
         const int32_t nch = (nU + K4U_CB - 1) / K4U_CB;
         mbar_arrive(bar(kTblEmpty + buf));
-        if (!mbar_wait(bar(kQFull), uc & 1, a.wait_ns, abort_flag, kSuspendNs)) break;
-        for (int32_t j = 0; j < nch && ok; ++j) {
+        if (!mbar_wait(bar(kQFull), uc & 1, a.wait_ns, abort_flag, kSuspendNs) || !s_wait(kc)) break;
+        issue_s(kc);
+        // the unit's first P.V overwrites O: the previous unit's O must have been read out
+        if (uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) break;
+        for (int32_t j = 1; j < nch; ++j) {
           const uint32_t c = kc + (uint32_t)j;
-          if (!mbar_wait(bar(kKFull + (c & 1)), (c >> 1) & 1, a.wait_ns, abort_flag, kSuspendNs) ||
-              (c >= 1 && !mbar_wait(bar(kSFree), (c - 1) & 1, a.wait_ns, abort_flag, kSuspendNs))) {
+          // S(c), then O(c - 1); O's inputs are tested before S goes out, so that the test's
+          // latency hides behind S's issue
+          if (!s_wait(c)) {
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t kb = sb0 + K4U_K_OFF + (c & 1) * K4U_SLOT;
-#pragma unroll
-          for (int ks = 0; ks < 12; ++ks)
-            tc_mma_ts(tmem + K4U_COL_S, tmem + K4U_COL_Q + 8 * ks,
-                      smem_desc_k_sw128_sbo(kb + (ks >> 2) * 1024 + (ks & 3) * 32, 3072), id_s, ks > 0 ? 1u : 0u);
-          tc_commit(bar(kKEmpty + (c & 1)));
-          tc_commit(bar(kSFull));
-          if (j == nch - 1) tc_commit(bar(kQEmpty));
-          if (j >= 1) {
-            if (j == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) {
-              ok = false;
-              break;
-            }
-            if (!issue_o(c - 1, j == 1)) ok = false;
+          const bool ro = o_ready(c - 1);
+          issue_s(c);
+          if (!ro && !o_wait(c - 1)) {
+            ok = false;
+            break;
           }
+          issue_o(c - 1, j == 1);
         }
         if (!ok) break;
-        if (nch == 1 && uc >= 1 && !mbar_wait(bar(kOEmpty), (uc - 1) & 1, a.wait_ns, abort_flag, kSuspendNs)) break;
-        if (!issue_o(kc + (uint32_t)nch - 1, nch == 1)) break;
+        const uint32_t cl = kc + (uint32_t)nch - 1;
+        if (!o_wait(cl)) break;
+        issue_o(cl, nch == 1);
         kc += (uint32_t)nch;
       }
       tc_commit(bar(kFinal));
@@ -519,7 +536,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         const uint32_t mine = (rb_row[j >> 1] >> ((uint32_t)(j & 1) * 16)) & 0xFFFFu;  // warp-uniform
         const int32_t ownj = own_r - j * K4U_CB;  // own block's slot in this chunk, if 0..15
         float s[64];
-        if (wait_ok(kSFull, c & 1)) {
+        if (wait_ok(kKEmpty + (c & 1), (c >> 1) & 1)) {
           tc_fence_after();
           uint32_t v0[32], v1[32];
           tmem_ld_16x256b_x8(tS16, v0);
@@ -588,7 +605,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
           ma = na;
           mb = nb;
           // O holds this unit's earlier chunks: rescale the row once O(c-1) is complete
-          if (j > 0 && wait_ok(kPvDone, (c - 1) & 1)) {
+          if (j > 0 && wait_ok(kVEmpty + ((c - 1) & 1), ((c - 1) >> 1) & 1)) {
             tc_fence_after();
 #pragma unroll 1
             for (int cc = 0; cc < 6; ++cc) {
@@ -607,7 +624,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
         la += lca;
         lb += lcb;
         // the P columns are free once O(c-1) has read them
-        if ((c == 0 || wait_ok(kPvDone, (c - 1) & 1)) && !bad) {
+        if ((c == 0 || wait_ok(kVEmpty + ((c - 1) & 1), ((c - 1) >> 1) & 1)) && !bad) {
           tc_fence_after();
           tmem_st_16x128b_x16(tP16, pw);
           tmem_st_wait();
@@ -633,7 +650,8 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       kc += (uint32_t)nch;
       // the next unit's Q goes in now: its first S overlaps this epilogue
       const int64_t un = u + gridDim.x;
-      if (un < n_units && wait_ok(kQEmpty, uc & 1)) {
+      // Q is free once the unit's last S is done, which this warp waited for in the chunk loop
+      if (un < n_units && !bad) {
         tc_fence_after();
         write_q(un);
       }
@@ -644,7 +662,7 @@ __global__ void __launch_bounds__(K4U_THREADS, 1)
       if (sync_stop()) break;
       const float lt = xl[m], mt = xm[m];
       if (hf == 0 && row_ok && a.lse) a.lse[hb] = (mt + __log2f(lt)) * 0.6931471805599453f;
-      if (!wait_ok(kPvDone, (kc - 1) & 1)) continue;  // caught at the next unit's barrier
+      if (!wait_ok(kVEmpty + ((kc - 1) & 1), ((kc - 1) >> 1) & 1)) continue;  // caught at the next unit's barrier
       tc_fence_after();
       const float inv = lt > 0.f ? __frcp_rn(lt) : 0.f;
       const float kLog2e = 1.4426950408889634f;
