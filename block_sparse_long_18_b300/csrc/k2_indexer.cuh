@@ -17,9 +17,19 @@
 //   warp 1      allocates 256 TMEM columns (two 128x128 fp32 accumulators) and issues
 //               tcgen05.mma kind::f16 (M=128, N=128, K=16) from one thread; commits free
 //               the B stage and publish the accumulator.
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns, write a swizzled 32x32 fp32
-//               tile to shared memory, TMA-store it (the store clips rows past the call's
-//               rows and columns past the workspace row length).
+//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns (thread = query row), then by
+//               mode:
+//               K2_SCORES    write a swizzled 32x32 fp32 tile to shared memory and TMA-store
+//                            it (the store clips rows past the call's rows and columns past
+//                            the workspace row length);
+//               K2_MAXIMA    per row, the largest score key of each 8 consecutive candidates
+//                            below the row's own block (a 4-byte key per 8 scores);
+//               K2_SURVIVORS per row, the candidates whose score key reaches the row's bound:
+//                            their keys, in place, and a mask word per 32 candidates;
+//                            nothing else leaves the SM.
+// The last two serve the top-k without materialising the scores: the (k-1)-th largest of a
+// row's group maxima is at most its (k-1)-th largest score (those maxima are k-1 distinct
+// candidates), so every block the top-k keeps, ties included, reaches that bound.
 // Every wait is bounded (globaltimer); on expiry the CTA raises an abort flag, drains the
 // copies and MMAs it has in flight, frees TMEM and returns.
 #pragma once
@@ -39,7 +49,24 @@ struct K2Args {
   int64_t n_items;      // G * n_mtiles * items_per_m
   int64_t ld;           // score row length of the workspace (elements)
   uint64_t wait_ns;
+  int32_t mode;         // K2_SCORES, K2_MAXIMA or K2_SURVIVORS
+  // K2_SCORES: with tile_flag, only the (group, 128-row tile) items whose flag is set
+  const int32_t* tile_flag;  // [G, n_mtiles] or null
+  // K2_MAXIMA: maxima[(g * Tc + row) * ld8 + j] = largest key of candidates 8j .. 8j+7 below
+  // the row's own block (only groups with at least one such candidate are written; 0 for
+  // a group's candidates past it); ld8 = 4 * ceil(ld / 32)
+  uint32_t* maxima;
+  int64_t ld8;
+  // K2_SURVIVORS, row r = g * Tc + row: bit u of smask[r * ld32 + x / 32] set for candidate
+  // x = 32 (x / 32) + u when its key reaches thr[r] (words of candidates below the row's own
+  // block only), and that key at skeys[r * ld + x]
+  const uint32_t* thr;
+  uint32_t* smask;
+  int64_t ld32;
+  uint32_t* skeys;
 };
+
+enum K2Mode : int { K2_SCORES = 0, K2_MAXIMA = 1, K2_SURVIVORS = 2 };
 
 constexpr int K2_THREADS = 192;
 constexpr uint32_t K2_TILE_BYTES = 128 * 128;            // 128 rows x 128 B (64 bf16)
@@ -65,6 +92,7 @@ __device__ __forceinline__ bool k2_decode_item(const K2Args& a, int64_t item, K2
   const int32_t nt = (int32_t)((ncand + 127) / 128);
   it.n_begin = c * a.nti;
   it.n_end = it.n_begin + a.nti < nt ? it.n_begin + a.nti : nt;
+  if (a.tile_flag && a.tile_flag[(int64_t)it.g * a.n_mtiles + it.m] == 0) return false;
   return it.n_begin < it.n_end;
 }
 
@@ -202,34 +230,70 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
         const uint32_t acc = it_acc & 1;
         if (!mbar_wait(bar_acc_full0 + 8 * acc, (it_acc >> 1) & 1, a.wait_ns, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        for (int c = 0; c < 4; ++c) {
-          // A 32x32 box wholly past the workspace row or the call's rows is never read:
-          // skip it entirely (warp-uniform), so only real stores cycle the two buffers.
-          const int32_t x0 = n * 128 + c * 32, y0 = it.m * 128 + (int32_t)q * 32;
-          if (x0 >= a.ld || y0 >= a.Tc) continue;
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + acc * 128 + c * 32, r);
-          tmem_ld_wait();
-          const uint32_t sb = n_store & 1;
-          const uint32_t stage_addr = sbase + K2_C_OFF + (e * 2 + sb) * 4096;
-          // the store issued from this buffer two stores ago must have finished reading it
-          if (lane == 0) bulk_wait_group_read<1>();
-          __syncwarp();
-          const uint32_t row_addr = stage_addr + lane * 128;
+        if (a.mode == K2_SCORES) {
+          for (int c = 0; c < 4; ++c) {
+            // A 32x32 box wholly past the workspace row or the call's rows is never read:
+            // skip it entirely (warp-uniform), so only real stores cycle the two buffers.
+            const int32_t x0 = n * 128 + c * 32, y0 = it.m * 128 + (int32_t)q * 32;
+            if (x0 >= a.ld || y0 >= a.Tc) continue;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + acc * 128 + c * 32, r);
+            tmem_ld_wait();
+            const uint32_t sb = n_store & 1;
+            const uint32_t stage_addr = sbase + K2_C_OFF + (e * 2 + sb) * 4096;
+            // the store issued from this buffer two stores ago must have finished reading it
+            if (lane == 0) bulk_wait_group_read<1>();
+            __syncwarp();
+            const uint32_t row_addr = stage_addr + lane * 128;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const uint32_t dst = row_addr + ((u ^ (lane & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(r[4 * u]), "r"(r[4 * u + 1]),
-                         "r"(r[4 * u + 2]), "r"(r[4 * u + 3])
-                         : "memory");
+            for (int u = 0; u < 8; ++u) {
+              const uint32_t dst = row_addr + ((u ^ (lane & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "r"(r[4 * u]), "r"(r[4 * u + 1]),
+                           "r"(r[4 * u + 2]), "r"(r[4 * u + 3])
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_3d(&tmC, stage_addr, x0, y0, it.g);
+              bulk_commit_group();
+            }
+            ++n_store;
           }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tmC, stage_addr, x0, y0, it.g);
-            bulk_commit_group();
+        } else {
+          // thread = query row of the tile; its candidates are the blocks below its own
+          const int64_t row = (int64_t)it.m * 128 + q * 32 + lane;
+          const int64_t bt = row < a.Tc ? (a.pos0 + row) / a.B : 0;
+          const int64_t rr = (int64_t)it.g * a.Tc + row;
+          const uint32_t thr = (a.mode == K2_SURVIVORS && row < a.Tc) ? a.thr[rr] : 0u;
+          for (int c = 0; c < 4; ++c) {
+            const int64_t x0 = (int64_t)n * 128 + c * 32;
+            if (x0 >= a.ld || (int64_t)it.m * 128 + q * 32 >= a.Tc) continue;  // warp-uniform
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + acc * 128 + c * 32, r);
+            tmem_ld_wait();
+            if (x0 >= bt) continue;  // no candidate of this row here
+            if (a.mode == K2_MAXIMA) {
+              uint32_t mx[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+              for (int u = 0; u < 32; ++u)
+                if (x0 + u < bt) mx[u >> 3] = max(mx[u >> 3], score_key(__uint_as_float(r[u])));
+              // groups 8j .. 8j+7 with j = x0/8 .. x0/8+3; x0 is a multiple of 32, so 16-byte aligned
+              *reinterpret_cast<uint4*>(a.maxima + rr * a.ld8 + x0 / 8) = make_uint4(mx[0], mx[1], mx[2], mx[3]);
+            } else {
+              uint32_t m = 0u;
+              uint32_t* krow = a.skeys + rr * a.ld;
+#pragma unroll
+              for (int u = 0; u < 32; ++u) {
+                const uint32_t kk = score_key(__uint_as_float(r[u]));
+                if (x0 + u < bt && kk >= thr) {
+                  m |= 1u << u;
+                  krow[x0 + u] = kk;
+                }
+              }
+              a.smask[rr * a.ld32 + x0 / 32] = m;
+            }
           }
-          ++n_store;
         }
         tc_fence_before();
         __syncwarp();

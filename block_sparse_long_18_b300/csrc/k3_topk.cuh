@@ -48,23 +48,32 @@ struct K3Args {
   int32_t* pair_cnt;    // [G * rows, nseg] entries each segment kept
   int32_t nseg;         // segments per row
   int32_t prefetch_ctas;  // a CTA warms L2 for the scores of CTA blockIdx.x + prefetch_ctas (0: off)
+  // bound-filtered selection (K3_THRESHOLD, K3_SELECT; row r = g * rows + i):
+  const uint32_t* keys_in;  // K3_THRESHOLD: group-maximum keys [G * rows, keys_ld], ceil(b_t / 8) per row
+  int64_t keys_ld;
+  uint32_t* thr_out;        // K3_THRESHOLD: bound per row (0: none)
+  const uint32_t* smask;    // K3_SELECT: survivor bits [G * rows, ld32], one per candidate below b_t
+  int64_t ld32;
+  const uint32_t* skeys;    // K3_SELECT: the survivors' keys at their candidate index [G * rows, ld]
+  int32_t cap;              // K3_SELECT: survivors a row may have (K3_SEL_CAP)
+  int32_t n_mtiles;         // K3_SELECT: 128-row tiles per group of the launch
+  int32_t* row_flag;        // K3_SELECT: set for a row whose survivors passed cap
+  int32_t* tile_flag;       //   and for its (group, 128-row tile)
+  const int32_t* only_flagged;  // K3_DIRECT / _SEGMENT / _MERGE: serve only rows whose flag is set
   int64_t pos[256];     // decode: absolute position of each row's query
 };
 
 // What a k3_topk launch reads and writes.
 enum K3Mode : int {
-  K3_DIRECT = 0,  // candidates = the row's scores; writes the final selection
-  K3_SEGMENT = 1, // candidates = one segment of the row's scores; writes (key, index) pairs
-  K3_MERGE = 2    // candidates = the row's segment pairs; writes the final selection
+  K3_DIRECT = 0,     // candidates = the row's scores; writes the final selection
+  K3_SEGMENT = 1,    // candidates = one segment of the row's scores; writes (key, index) pairs
+  K3_MERGE = 2,      // candidates = the row's segment pairs; writes the final selection
+  K3_THRESHOLD = 3,  // candidates = the row's group maxima; writes the (k-1)-th largest (a bound)
+  K3_SELECT = 4      // candidates = the row's survivors of that bound (mask bits and keys in
+                     // place); writes the final selection
 };
+constexpr int K3_SEL_CAP = 4096;  // survivors a K3_SELECT row may hold (128 threads x 32)
 
-// Order-preserving unsigned key of a score.  Adding +0 turns -0 into +0 (round to
-// nearest; denormals are kept, the library is built without flush-to-zero), then negative
-// values have all bits flipped and non-negative ones the sign bit set.
-__device__ __forceinline__ uint32_t score_key(float f) {
-  const uint32_t u = __float_as_uint(f + 0.0f);
-  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
-}
 
 // Inclusive warp scan.
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -108,8 +117,10 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   __shared__ uint32_t wsum[2][NW];
   __shared__ uint32_t jw_cnt[NJ * NW];  // counts per (group j, warp), then their exclusive scan
   __shared__ uint32_t sh_digit, sh_above, sh_eq;
-  __shared__ uint32_t bitmap[STREAM ? 1 : NT * PER / 32];  // kept slots
-  __shared__ uint32_t tiemap[STREAM ? 1 : NT * PER / 32];  // slots equal to the threshold key
+  constexpr bool BITMAP = !STREAM && MODE != K3_THRESHOLD;
+  __shared__ uint32_t bitmap[BITMAP ? NT * PER / 32 : 1];  // kept slots
+  __shared__ uint32_t tiemap[BITMAP ? NT * PER / 32 : 1];  // slots equal to the threshold key
+  __shared__ int32_t sel_list[MODE == K3_SELECT ? NT * PER : 1];  // K3_SELECT: survivor index of each slot
 
   constexpr int SEGLEN = NT * PER;  // candidates per segment (K3_SEGMENT)
   const int64_t r = MODE == K3_SEGMENT ? blockIdx.x / a.nseg : blockIdx.x;  // (group, row) of the launch
@@ -124,9 +135,10 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   const float* row = a.scores + (g * a.rows + i) * a.ld;
   const int tid = threadIdx.x;
   const uint32_t lane = tid & 31, warp = tid >> 5;
+  if (a.only_flagged && a.only_flagged[r] == 0) return;
   // Warm L2 for the scores of the CTA about two waves later (launched when a CTA of this
   // wave retires), one 128-byte line per thread, so that its row load hits L2.
-  if (MODE != K3_MERGE && !STREAM && a.prefetch_ctas > 0) {
+  if ((MODE == K3_DIRECT || MODE == K3_SEGMENT) && !STREAM && a.prefetch_ctas > 0) {
     const int64_t cb = (int64_t)blockIdx.x + a.prefetch_ctas;
     const int64_t nseg2 = MODE == K3_SEGMENT ? a.nseg : 1;
     if (cb < (int64_t)a.G * a.rows * nseg2) {
@@ -150,6 +162,12 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     if (n < 0) n = 0;
   } else if (MODE == K3_MERGE) {
     n = pstride;
+  } else if (MODE == K3_THRESHOLD) {
+    n = (bt + 7) / 8;  // groups of 8 candidates below the own block
+    if (n <= need) {   // fewer group maxima than blocks to keep: no bound
+      if (tid == 0) a.thr_out[r] = 0u;
+      return;
+    }
   }
 
   if (need == 0) {  // k = 1: the own block alone (segmented launches are never made for k = 1)
@@ -170,7 +188,7 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
       if (tid == 0) a.pair_cnt[r * a.nseg + seg] = (int32_t)n;
       return;
     }
-  } else if (bt <= need) {  // every causal block is kept
+  } else if (MODE != K3_THRESHOLD && bt <= need) {  // every causal block is kept
     for (int64_t j = tid; j < a.k; j += NT) out[j] = j < bt ? (int32_t)j : (j == bt ? (int32_t)bt : -1);
     if (tid == 0) a.sel_cnt[g * a.T_out + a.out_row0 + i] = (int32_t)(bt + 1);
     return;
@@ -180,14 +198,50 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   // candidate index of key e of group j in tile `tile`
   auto kidx = [&](int tile, int j, int e) -> int32_t { return tile * TILE + 4 * (j * NT + tid) + e; };
   uint32_t key[PER];
-  const uint32_t* mkeys = a.pair_key + r * pstride;  // K3_MERGE input (key 0 in unused slots)
+  const uint32_t* mkeys = MODE == K3_THRESHOLD ? a.keys_in + r * a.keys_ld : a.pair_key + r * pstride;
+  if (MODE == K3_SELECT) {
+    // The survivors' candidate indices, in index order, from the mask words: thread tid
+    // scans words [tid W, tid W + W), one block scan places its survivors.
+    const uint32_t* mrow = a.smask + r * a.ld32;
+    const int64_t n_words = (bt + 31) / 32;
+    const int64_t W = (n_words + NT - 1) / NT;
+    uint32_t c = 0;
+    for (int64_t w = 0; w < W; ++w) {
+      const int64_t wi = (int64_t)tid * W + w;
+      if (wi < n_words) c += (uint32_t)__popc(__ldg(mrow + wi));
+    }
+    uint32_t total;
+    uint32_t o = k3_block_excl_scan<NT>(c, warp_tot, total);
+    if (total > (uint32_t)a.cap) {  // more survivors than one CTA holds: redone from the scores
+      if (tid == 0) {
+        a.row_flag[r] = 1;
+        a.tile_flag[g * a.n_mtiles + i / 128] = 1;
+      }
+      return;
+    }
+    for (int64_t w = 0; w < W; ++w) {
+      const int64_t wi = (int64_t)tid * W + w;
+      uint32_t bits = wi < n_words ? __ldg(mrow + wi) : 0u;
+      while (bits != 0u) {
+        const uint32_t b = (uint32_t)__ffs(bits) - 1u;
+        bits &= bits - 1u;
+        sel_list[o++] = (int32_t)(wi * 32 + b);
+      }
+    }
+    __syncthreads();
+    n = total;
+  }
+  const uint32_t* srow = a.skeys + r * a.ld;  // K3_SELECT: keys at candidate indices
   auto load_tile = [&](int tile) {
 #pragma unroll
     for (int j = 0; j < NJ; ++j) {
       const int32_t b = kidx(tile, j, 0);
-      if (MODE == K3_MERGE) {
+      if (MODE == K3_MERGE || MODE == K3_THRESHOLD) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) key[4 * j + e] = (b + e < n) ? __ldg(mkeys + b + e) : 0u;
+      } else if (MODE == K3_SELECT) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) key[4 * j + e] = b + e < n ? __ldg(srow + sel_list[b + e]) : 0u;
       } else if (b + 3 < n && ((base + b) & 3) == 0) {
         const float4 f = __ldg(reinterpret_cast<const float4*>(row + base + b));
         key[4 * j] = score_key(f.x);
@@ -231,7 +285,7 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     hist2[0][b] = 0;
     hist2[1][b] = 0;
   }
-  if (!STREAM) {
+  if (BITMAP) {
     for (int w = tid; w < NT * PER / 32; w += NT) {
       bitmap[w] = 0;
       tiemap[w] = 0;
@@ -297,6 +351,13 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
     if (need_rem == eq_count) break;  // the whole bucket is kept: no tie to break
   }
 
+  if (MODE == K3_THRESHOLD) {
+    // The (k-1)-th largest maximum, or (the loop stopped at a bucket kept whole) the
+    // bucket's lower end, which is at most that maximum: either is a bound.
+    if (tid == 0) a.thr_out[r] = prefix;
+    return;
+  }
+
   // ---- compaction in ascending index order ----
   // A key is kept if its masked value exceeds the prefix, or equals it and its rank among
   // the equal keys (in index order) is at least `skip`.  Without ties to break (skip = 0,
@@ -339,6 +400,8 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
           a.pair_idx[r * pstride + (int64_t)seg * need + o] = (int32_t)(base + slot);
         } else if (MODE == K3_MERGE) {
           out[o] = __ldg(a.pair_idx + r * pstride + slot);
+        } else if (MODE == K3_SELECT) {
+          out[o] = sel_list[slot];
         } else {
           out[o] = slot;
         }

@@ -411,6 +411,14 @@ __device__ __forceinline__ float fast_rcp(float x) {
   return y;
 }
 
+// Order-preserving unsigned key of a score.  Adding +0 turns -0 into +0 (round to
+// nearest; denormals are kept, the library is built without flush-to-zero), then negative
+// values have all bits flipped and non-negative ones the sign bit set.
+__device__ __forceinline__ uint32_t score_key(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u);
+}
+
 // ------------------------------------------------------------------------------------
 // cp.async (16-byte, L2 only)
 // ------------------------------------------------------------------------------------

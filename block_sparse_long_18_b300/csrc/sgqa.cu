@@ -195,13 +195,31 @@ int64_t k3_segments(const Prm& p, int64_t max_cand) {
   return nseg * (p.k - 1) <= kK3RegRow ? nseg : 0;
 }
 
+// The bound-filtered top-k (indexer maxima -> bound -> survivors -> selection, the scores
+// never written) can serve rows of up to 8 * kK3RegRow candidates (their group maxima fit
+// one register-resident CTA), with k - 1 at most the survivor capacity; a row needs more
+// than 8 (k - 1) candidates for a bound (fewer group maxima than blocks to keep give none).
+// It runs the indexer's MMAs twice, which pays only for rows longer than one CTA's
+// registers hold (kK3RegRow), where the plain top-k needs its segment + merge pair
+// (measured on B300: the 1M chunk's indexer + top-k 15.6 -> 9.6 ms; rows of 16K
+// candidates about break even).
+int64_t filtered_min_cand(const Prm& p) { return std::max<int64_t>(8 * (int64_t)(p.k - 1), kK3RegRow); }
+bool filtered_topk_fits(const Prm& p, int64_t max_cand) {
+  return p.k >= 2 && p.k - 1 <= K3_SEL_CAP && max_cand <= 8 * kK3RegRow && max_cand > filtered_min_cand(p);
+}
+
 // Layout of the top-k workspace for `rows` rows: fp32 scores [G, rows, ld], then (for
 // segmented rows) pair keys and indices [G * rows, nseg * (k-1)] and counts [G * rows, nseg].
+// With `filtered`: group maxima [G * rows, ld8], bounds [G * rows], survivor masks
+// [G * rows, ld32], then the flags of rows with more survivors than K3_SEL_CAP [G * rows]
+// and of their 128-row tiles [G, n_mtiles] (one memset clears them per pass).  The score
+// buffer holds the survivors' keys in place, and the scores of flagged tiles.
 struct IndexWs {
-  int64_t ld, nseg;
-  size_t scores, pair_key, pair_idx, pair_cnt, total;  // byte offsets and size
+  int64_t ld, nseg, ld8, ld32, n_mtiles;
+  bool filtered;
+  size_t scores, pair_key, pair_idx, pair_cnt, maxima, thr, smask, flags, total;
 };
-IndexWs index_ws_layout(const Prm& p, int64_t rows, int64_t max_cand) {
+IndexWs index_ws_layout(const Prm& p, int64_t rows, int64_t max_cand, bool filtered) {
   IndexWs w{};
   w.ld = std::max<int64_t>(4, (int64_t)align_up((size_t)max_cand, 4));
   w.nseg = k3_segments(p, max_cand);
@@ -211,6 +229,17 @@ IndexWs index_ws_layout(const Prm& p, int64_t rows, int64_t max_cand) {
   w.pair_idx = w.pair_key + align_up(r * w.nseg * (p.k - 1) * 4, 256);
   w.pair_cnt = w.pair_idx + align_up(r * w.nseg * (p.k - 1) * 4, 256);
   w.total = w.pair_cnt + align_up(r * w.nseg * 4, 256);
+  if (filtered) {
+    w.filtered = true;
+    w.ld8 = 4 * cdiv(w.ld, 32);
+    w.ld32 = cdiv(w.ld, 32);
+    w.n_mtiles = cdiv(rows, 128);
+    w.maxima = w.total;
+    w.thr = w.maxima + align_up(r * w.ld8 * 4, 256);
+    w.smask = w.thr + align_up(r * 4, 256);
+    w.flags = w.smask + align_up(r * w.ld32 * 4, 256);
+    w.total = w.flags + align_up(r * 4 + (size_t)p.G * w.n_mtiles * 4, 256);
+  }
   return w;
 }
 
@@ -220,19 +249,20 @@ IndexWs index_ws_layout(const Prm& p, int64_t rows, int64_t max_cand) {
 // Register-resident top-k launch for rows of at most NT * PER candidates, PER the
 // smallest multiple of 4 that holds max_cand (at least 8): short rows do not pay for
 // empty slots.
-template <int NT>
+template <int NT, int MODE = K3_DIRECT>
 void launch_k3_regs(const K3Args& a, int64_t max_cand, int64_t grid, cudaStream_t st) {
   const int per = (int)std::max<int64_t>(8, cdiv(cdiv(max_cand, NT), 4) * 4);
   switch (per) {
-    case 8: k3_topk<NT, 8, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
-    case 12: k3_topk<NT, 12, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
-    case 16: k3_topk<NT, 16, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
-    case 20: k3_topk<NT, 20, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
-    case 24: k3_topk<NT, 24, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
-    case 28: k3_topk<NT, 28, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
-    default: k3_topk<NT, 32, false><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 8: k3_topk<NT, 8, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 12: k3_topk<NT, 12, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 16: k3_topk<NT, 16, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 20: k3_topk<NT, 20, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 24: k3_topk<NT, 24, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    case 28: k3_topk<NT, 28, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
+    default: k3_topk<NT, 32, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
   }
 }
+static_assert(K3_SEL_CAP == 128 * 32, "survivor selection: 128 threads x 32 keys");
 
 // One CTA per row; the block is the smallest whose registers (up to 32 keys per thread)
 // hold the launch's longest row.  Longer rows go through the segment + merge pair when
@@ -245,7 +275,7 @@ cudaError_t launch_k3(K3Args a, int64_t max_cand, uint8_t* ws, const IndexWs& ws
   if (grid <= 0) return cudaSuccess;
   // prefetch distance: resident CTAs (1,024 threads per SM) times the waves ahead (one
   // wave measured best on B300: 128K indexer + top-k 16.97 -> 16.46 ms; two 16.50, four 17.50)
-  {
+  if (!a.only_flagged) {
     const int nt = max_cand <= 128 * kK3Per ? 128 : (max_cand <= 256 * kK3Per ? 256 : kK3Threads);
     a.prefetch_ctas = SGQA_K3_PREFETCH_WAVES * num_sms() * (1024 / nt);
   }
@@ -287,26 +317,35 @@ cudaError_t launch_k1(const K1Args& a, cudaStream_t st, bool e4m3 = false) {
 
 // Bytes of the indexer + top-k workspace for `rows` query rows whose largest candidate
 // count is max_cand.
-size_t index_ws_bytes(const Prm& p, int64_t rows, int64_t max_cand) { return index_ws_layout(p, rows, max_cand).total; }
+size_t index_ws_bytes(const Prm& p, int64_t rows, int64_t max_cand, bool filtered) {
+  return index_ws_layout(p, rows, max_cand, filtered).total;
+}
+// what a prefill's indexer + top-k asks for: the filtered layout where it can serve
+size_t index_ws_bytes(const Prm& p, int64_t rows, int64_t max_cand) {
+  return index_ws_bytes(p, rows, max_cand, filtered_topk_fits(p, max_cand));
+}
 
 // ---- the indexer + top-k over rows [0, T) at positions q_start .. ----
 sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t q_start, const void* k_blk,
                            int64_t nb_cap, int32_t* sel_idx, int32_t* sel_cnt, void* ws, size_t ws_bytes,
                            cudaStream_t st) {
   const int64_t max_cand = (q_start + T - 1) / p.B;  // candidates of the last row
-  // rows per pass: as many as the workspace holds, preferring kIndexChunkRows
+  // rows per pass: as many as the workspace holds, preferring kIndexChunkRows; the
+  // bound-filtered top-k when the workspace holds its buffers for kIndexChunkRows rows
   int64_t rows = std::min<int64_t>(T, kIndexChunkRows);
-  if (index_ws_bytes(p, rows, max_cand) > ws_bytes) {
+  const bool filtered = filtered_topk_fits(p, max_cand) && index_ws_bytes(p, rows, max_cand, true) <= ws_bytes;
+  if (!filtered && index_ws_bytes(p, rows, max_cand, false) > ws_bytes) {
     int64_t lo = 0, hi = rows;  // largest row count that fits
     while (lo < hi) {
       const int64_t mid = (lo + hi + 1) / 2;
-      if (index_ws_bytes(p, mid, max_cand) <= ws_bytes) lo = mid; else hi = mid - 1;
+      if (index_ws_bytes(p, mid, max_cand, false) <= ws_bytes) lo = mid; else hi = mid - 1;
     }
     rows = lo >= 128 ? lo / 128 * 128 : lo;
     if (rows < std::min<int64_t>(T, 128)) return SGQA_ERR_WORKSPACE_TOO_SMALL;
   }
   if (!aligned16(ws)) return SGQA_ERR_INVALID_ARGUMENT;
-  const IndexWs wsl = index_ws_layout(p, rows, max_cand);
+  const IndexWs wsl = index_ws_layout(p, rows, max_cand, filtered);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
   const int64_t ld = wsl.ld;
   float* scores = static_cast<float*>(ws);
 
@@ -321,27 +360,27 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
   for (int64_t r0 = 0; r0 < T; r0 += rows) {
     const int64_t rc = std::min<int64_t>(rows, T - r0);
     const int64_t cand_last = (q_start + r0 + rc - 1) / p.B;
-    if (cand_last > 0) {
-      CUtensorMap tc;
-      if (!make_map_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scores, ld, rc, p.G, (uint64_t)ld * 4,
-                       (uint64_t)rc * ld * 4, 32, 32, 1))
-        return SGQA_ERR_CUDA;
-      K2Args a2{};
-      a2.G = p.G;
-      a2.P = p.P;
-      a2.B = p.B;
-      a2.kch = p.P / 64;
-      a2.Tc = rc;
-      a2.row_base = r0;
-      a2.pos0 = q_start + r0;
-      a2.n_mtiles = (int32_t)cdiv(rc, 128);
-      a2.nti = 8;
-      a2.items_per_m = (int32_t)cdiv(cdiv(cand_last, 128), a2.nti);
-      a2.n_items = (int64_t)p.G * a2.n_mtiles * a2.items_per_m;
-      a2.ld = ld;
-      a2.wait_ns = g_wait_ns;
-      SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
-    }
+    // the pass runs bound-filtered when every row has more than filtered_min_cand candidates
+    const bool pass_filtered = wsl.filtered && (q_start + r0) / p.B > filtered_min_cand(p);
+    CUtensorMap tc;
+    if (cand_last > 0 && !make_map_3d(&tc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scores, ld, rc, p.G, (uint64_t)ld * 4,
+                                      (uint64_t)rc * ld * 4, 32, 32, 1))
+      return SGQA_ERR_CUDA;
+    K2Args a2{};
+    a2.G = p.G;
+    a2.P = p.P;
+    a2.B = p.B;
+    a2.kch = p.P / 64;
+    a2.Tc = rc;
+    a2.row_base = r0;
+    a2.pos0 = q_start + r0;
+    a2.n_mtiles = (int32_t)cdiv(rc, 128);
+    a2.nti = 8;
+    a2.items_per_m = (int32_t)cdiv(cdiv(cand_last, 128), a2.nti);
+    a2.n_items = (int64_t)p.G * a2.n_mtiles * a2.items_per_m;
+    a2.ld = ld;
+    a2.wait_ns = g_wait_ns;
+    a2.mode = K2_SCORES;
     K3Args a3{};
     a3.scores = scores;
     a3.ld = ld;
@@ -355,7 +394,66 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
     a3.sel_idx = sel_idx;
     a3.sel_cnt = sel_cnt;
     a3.use_pos = 0;
-    SGQA_CUDA_OK(launch_k3(a3, cand_last, static_cast<uint8_t*>(ws), wsl, st));
+    if (pass_filtered) {
+      const int64_t rr = (int64_t)p.G * rc;
+      uint32_t* maxima = reinterpret_cast<uint32_t*>(wsb + wsl.maxima);
+      uint32_t* thr = reinterpret_cast<uint32_t*>(wsb + wsl.thr);
+      uint32_t* smask = reinterpret_cast<uint32_t*>(wsb + wsl.smask);
+      int32_t* row_flag = reinterpret_cast<int32_t*>(wsb + wsl.flags);  // [G * rc]
+      int32_t* tile_flag = row_flag + rr;                                 // [G, n_mtiles of this pass]
+      SGQA_CUDA_OK(cudaMemsetAsync(row_flag, 0, (size_t)(rr + (int64_t)p.G * a2.n_mtiles) * 4, st));
+      // 1. group maxima of the scores (nothing else leaves the SM)
+      a2.mode = K2_MAXIMA;
+      a2.maxima = maxima;
+      a2.ld8 = wsl.ld8;
+      SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
+      // 2. each row's bound: the (k-1)-th largest of its group maxima
+      {
+        K3Args t = a3;
+        t.keys_in = maxima;
+        t.keys_ld = wsl.ld8;
+        t.thr_out = thr;
+        const int64_t n_max = cdiv(cand_last, 8), grid = rr;
+        if (n_max <= 128 * kK3Per)
+          launch_k3_regs<128, K3_THRESHOLD>(t, n_max, grid, st);
+        else if (n_max <= 256 * kK3Per)
+          launch_k3_regs<256, K3_THRESHOLD>(t, n_max, grid, st);
+        else
+          launch_k3_regs<kK3Threads, K3_THRESHOLD>(t, n_max, grid, st);
+        SGQA_CUDA_OK(cudaGetLastError());
+      }
+      // 3. the candidates that reach the bound: mask bits, keys in place
+      a2.mode = K2_SURVIVORS;
+      a2.thr = thr;
+      a2.smask = smask;
+      a2.ld32 = wsl.ld32;
+      a2.skeys = reinterpret_cast<uint32_t*>(scores);
+      SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
+      // 4. the exact selection over each row's survivors; a row past the capacity is flagged
+      {
+        K3Args t = a3;
+        t.smask = smask;
+        t.ld32 = wsl.ld32;
+        t.skeys = reinterpret_cast<const uint32_t*>(scores);
+        t.cap = K3_SEL_CAP;
+        t.n_mtiles = a2.n_mtiles;
+        t.row_flag = row_flag;
+        t.tile_flag = tile_flag;
+        k3_topk<128, 32, false, K3_SELECT><<<(unsigned)rr, 128, 0, st>>>(t);
+        SGQA_CUDA_OK(cudaGetLastError());
+      }
+      // 5. flagged rows (heavy ties) are redone from their scores: the indexer writes the
+      // flagged tiles' scores, the top-k serves the flagged rows; other CTAs return at once
+      a2.mode = K2_SCORES;
+      a2.tile_flag = tile_flag;
+      SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
+      a3.only_flagged = row_flag;
+      k3_topk<128, kK3Per, true><<<(unsigned)rr, 128, 0, st>>>(a3);  // any row length
+      SGQA_CUDA_OK(cudaGetLastError());
+      continue;
+    }
+    if (cand_last > 0) SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
+    SGQA_CUDA_OK(launch_k3(a3, cand_last, wsb, wsl, st));
   }
   return SGQA_OK;
 }
@@ -721,7 +819,7 @@ size_t sgqa_workspace_bytes(const sgqa_params* prm, int32_t op, int64_t T, int64
       return host_ws_layout(p, host_chunk_rows(p, T, batch), ctx_len).total;
     case SGQA_OP_DECODE: {
       if (batch < 1 || batch > kMaxBatch) return 0;
-      const size_t sc = index_ws_bytes(p, batch, max_cand);
+      const size_t sc = index_ws_bytes(p, batch, max_cand, false);
       const int nsplit = 32;
       const size_t po = align_up((size_t)p.G * batch * nsplit * 16 * 192 * 4, 256);
       const size_t pml = align_up((size_t)p.G * batch * nsplit * 16 * 2 * 4, 256);
@@ -796,7 +894,7 @@ sgqa_status sgqa_index_topk_noalloc(const sgqa_params* prm, const void* q_proxy,
   const int64_t max_cand = (q_start + T - 1) / p.B;
   if (max_cand > nb_cap || max_cand > (int64_t)INT32_MAX) return SGQA_ERR_INVALID_ARGUMENT;
   // the smallest pass must fit in the fixed scratch array
-  if (index_ws_bytes(p, std::min<int64_t>(T, 128), max_cand) > (size_t)SGQA_NOALLOC_SCRATCH_BYTES)
+  if (index_ws_bytes(p, std::min<int64_t>(T, 128), max_cand, false) > (size_t)SGQA_NOALLOC_SCRATCH_BYTES)
     return SGQA_ERR_WORKSPACE_TOO_SMALL;
   void* ws = nullptr;
   s = noalloc_scratch_address(&ws);
@@ -968,7 +1066,7 @@ static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64
     return SGQA_ERR_INVALID_ARGUMENT;
   const int64_t nb_total = total / p.B;
   const int64_t max_cand = (max_len - 1) / p.B;
-  const IndexWs wsl = index_ws_layout(p, batch, max_cand);
+  const IndexWs wsl = index_ws_layout(p, batch, max_cand, false);
   const int64_t ld = wsl.ld;
   uint8_t* w = static_cast<uint8_t*>(ws);
   float* scores = reinterpret_cast<float*>(w);

@@ -102,6 +102,15 @@ def test_workspace_sizes(lib):
     # 128K prefill: one pass of 8,192 rows x 4 groups x 16,384 fp32 candidates
     ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 131072, 131072)
     assert ws == 4 * 8192 * 16384 * 4
+    # the 1M limit (rows past 16,384 candidates): the scores (or the survivors' keys in place)
+    # [4 x 8,192 x 131,072], the segment + merge pair buffers (8 segments x 511 entries) of
+    # the plain top-k, then the bound-filtered top-k's group maxima (a key per 8
+    # candidates), bounds, survivor masks (a bit per candidate), row flags and 128-row tile
+    # flags
+    r = 4 * 8192
+    w1 = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 8192, 1 << 20)
+    seg = -(-r * 8 * 511 * 4 // 256) * 256
+    assert w1 == r * 131072 * 4 + 2 * seg + r * 8 * 4 + r * 16384 * 4 + r * 4 + r * 4096 * 4 + (r * 4 + 4 * 64 * 4)
     # prefill: the indexer's scratch, reused by the grouped attention's sort keys, row order
     # and unit lists (4 groups x 131,072 rows x 13.5 bytes)
     wa = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_ATTN, 131072, 131072)
