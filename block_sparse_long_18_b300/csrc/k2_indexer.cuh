@@ -17,8 +17,9 @@
 //   warp 1      allocates 256 TMEM columns (two 128x128 fp32 accumulators) and issues
 //               tcgen05.mma kind::f16 (M=128, N=128, K=16) from one thread; commits free
 //               the B stage and publish the accumulator.
-//   warps 2..5  epilogue: tcgen05.ld 32 lanes x 32 columns (thread = query row), then by
-//               mode:
+//   warps 2..9  epilogue, two warps per TMEM lane quarter, each taking two of a tile's four
+//               32-column chunks: tcgen05.ld 32 lanes x 32 columns (thread = query row), then
+//               by mode:
 //               K2_SCORES    write a swizzled 32x32 fp32 tile to shared memory and TMA-store
 //                            it (the store clips rows past the call's rows and columns past
 //                            the workspace row length);
@@ -68,11 +69,11 @@ struct K2Args {
 
 enum K2Mode : int { K2_SCORES = 0, K2_MAXIMA = 1, K2_SURVIVORS = 2 };
 
-constexpr int K2_THREADS = 192;
+constexpr int K2_THREADS = 320;
 constexpr uint32_t K2_TILE_BYTES = 128 * 128;            // 128 rows x 128 B (64 bf16)
 constexpr uint32_t K2_A_OFF = 0;                         // 4 chunks
 constexpr uint32_t K2_B_OFF = 4 * K2_TILE_BYTES;         // 2 stages x 4 chunks
-constexpr uint32_t K2_C_OFF = K2_B_OFF + 8 * K2_TILE_BYTES;  // 4 warps x 2 x 4 KB
+constexpr uint32_t K2_C_OFF = K2_B_OFF + 8 * K2_TILE_BYTES;  // 8 warps x 4 KB
 constexpr uint32_t K2_BAR_OFF = K2_C_OFF + 8 * 4096;
 constexpr uint32_t K2_SMEM_BYTES = K2_BAR_OFF + 128 + 1024;  // + alignment slack
 
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
       mbar_init(bar_b_full0 + 8 * s, 1);
       mbar_init(bar_b_empty0 + 8 * s, 1);
       mbar_init(bar_acc_full0 + 8 * s, 1);
-      mbar_init(bar_acc_empty0 + 8 * s, 4);
+      mbar_init(bar_acc_empty0 + 8 * s, 8);
     }
     mbar_init(bar_final, 1);
     *abort_flag = 0;
@@ -221,6 +222,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
     // ---------------- epilogue: TMEM -> smem -> TMA store ----------------
     const uint32_t q = warp & 3;          // TMEM lane quarter this warp may access
     const uint32_t e = warp - 2;          // staging slot
+    const int c0 = 2 * (int)(e >> 2);     // first of this warp's two 32-column chunks
     uint32_t it_acc = 0, n_store = 0;
     bool ok = true;
     for (int64_t item = blockIdx.x; item < a.n_items && ok; item += gridDim.x) {
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
         if (!mbar_wait(bar_acc_full0 + 8 * acc, (it_acc >> 1) & 1, a.wait_ns, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (a.mode == K2_SCORES) {
-          for (int c = 0; c < 4; ++c) {
+          for (int c = c0; c < c0 + 2; ++c) {
             // A 32x32 box wholly past the workspace row or the call's rows is never read:
             // skip it entirely (warp-uniform), so only real stores cycle the two buffers.
             const int32_t x0 = n * 128 + c * 32, y0 = it.m * 128 + (int32_t)q * 32;
@@ -239,10 +241,9 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
             uint32_t r[32];
             tmem_ld_32x32b_x32(tmem_base + ((q * 32) << 16) + acc * 128 + c * 32, r);
             tmem_ld_wait();
-            const uint32_t sb = n_store & 1;
-            const uint32_t stage_addr = sbase + K2_C_OFF + (e * 2 + sb) * 4096;
-            // the store issued from this buffer two stores ago must have finished reading it
-            if (lane == 0) bulk_wait_group_read<1>();
+            const uint32_t stage_addr = sbase + K2_C_OFF + e * 4096;
+            // this warp's previous store must have finished reading its buffer
+            if (lane == 0) bulk_wait_group_read<0>();
             __syncwarp();
             const uint32_t row_addr = stage_addr + lane * 128;
 #pragma unroll
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
           const int64_t bt = row < a.Tc ? (a.pos0 + row) / a.B : 0;
           const int64_t rr = (int64_t)it.g * a.Tc + row;
           const uint32_t thr = (a.mode == K2_SURVIVORS && row < a.Tc) ? a.thr[rr] : 0u;
-          for (int c = 0; c < 4; ++c) {
+          for (int c = c0; c < c0 + 2; ++c) {
             const int64_t x0 = (int64_t)n * 128 + c * 32;
             if (x0 >= a.ld || (int64_t)it.m * 128 + q * 32 >= a.Tc) continue;  // warp-uniform
             uint32_t r[32];
