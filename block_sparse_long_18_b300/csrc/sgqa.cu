@@ -203,7 +203,10 @@ int64_t k3_segments(const Prm& p, int64_t max_cand) {
 // registers hold (kK3RegRow), where the plain top-k needs its segment + merge pair
 // (measured on B300: the 1M chunk's indexer + top-k 15.6 -> 9.6 ms; rows of 16K
 // candidates about break even).
-int64_t filtered_min_cand(const Prm& p) { return std::max<int64_t>(8 * (int64_t)(p.k - 1), kK3RegRow); }
+#ifndef SGQA_K3_FILTER_MIN
+#define SGQA_K3_FILTER_MIN 16384
+#endif
+int64_t filtered_min_cand(const Prm& p) { return std::max<int64_t>(8 * (int64_t)(p.k - 1), SGQA_K3_FILTER_MIN); }
 bool filtered_topk_fits(const Prm& p, int64_t max_cand) {
   return p.k >= 2 && p.k - 1 <= K3_SEL_CAP && max_cand <= 8 * kK3RegRow && max_cand > filtered_min_cand(p);
 }

@@ -126,6 +126,13 @@ SGQA_API sgqa_status sgqa_build_block_index(const sgqa_params* prm, const void* 
  *   sel_cnt  [G, T]          int32, written
  *   ws       scratch of at least sgqa_workspace_bytes(prm, SGQA_OP_INDEX_TOPK, T,
  *            q_start + T, 1) bytes; a larger workspace lets more rows share one pass.
+ * Rows of more than 16,384 (and 8 (k - 1)) candidates, up to 131,072, are selected without
+ * writing their scores when the workspace holds that path's buffers for 8,192 rows (the
+ * size sgqa_workspace_bytes returns does): the indexer writes the largest score of every 8
+ * candidates, the (k-1)-th largest of those is a lower bound on the row's (k-1)-th score,
+ * and only the candidates that reach it (their keys, a bit each) go to the exact
+ * selection; a row with more than 4,096 of them is redone from its scores.  The selection
+ * is the same either way.
  * Errors: INVALID_ARGUMENT (nulls, q_start < 0, blocks beyond nb_cap),
  * WORKSPACE_TOO_SMALL, UNSUPPORTED_SHAPE.
  * ------------------------------------------------------------------------------- */
