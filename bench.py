@@ -86,6 +86,7 @@ _I64_MIN = -(1 << 63)
 
 
 GROUP_WINDOW = 4096  # rows per grouping window of the library's grouped attention mode
+FILTERED_MIN_CAND = 16384  # rows past this many candidates take the library's bound-filtered top-k
 
 
 def _murmur32(x):
@@ -470,6 +471,14 @@ def run_sgqa(args, rank, world, local_rank):
     # secondary: scores never leaving the SM (operands, selection out, FLOPs at peak)
     fused_floor = max(w["k2_flop"] / tf, (w["k2_bytes"] - k2_scores_bytes + 4 * wl.G * w["sum_n"]) / hbm_bps) * 1e3
     stages["k2k3_index_topk"]["fused_floor_ms"] = round(fused_floor, 4)
+    if wl.q_start // wl.B > FILTERED_MIN_CAND and (wl.q_start + wl.T - 1) // wl.B <= 8 * 16384:
+        # every row takes the library's bound-filtered path, which writes no score matrix:
+        # the stage's line is then the fused floor (its FLOPs at the bf16 peak, operands and
+        # selection once), not the materialised-score line
+        roof["k2k3_index_topk"] = fused_floor
+        stages["k2k3_index_topk"].update(
+            roofline_ms=round(fused_floor, 4), frac=round(fused_floor / ik_ms, 4),
+            bound="tensor (bound-filtered selection: no score matrix written; FLOPs of one indexer pass at the bf16 peak)")
     k4s = stages["k4_sparse_attn"]
     k4s["bound"] = "tensor" if w["k4_flop"] / tf >= k4_compulsory / hbm_bps else "hbm"
     k4s["useful_tflop"] = round(w["k4_flop"] / 1e12, 3)
