@@ -102,6 +102,8 @@ def test_workspace_sizes(lib):
     # 128K prefill: one pass of 8,192 rows x 4 groups x 16,384 fp32 candidates
     ws = lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 131072, 131072)
     assert ws == 4 * 8192 * 16384 * 4
+    # a 16K context (2,047 candidates at most): the same per-candidate layout
+    assert lib.sgqa_workspace_bytes(prm, lib.SGQA_OP_INDEX_TOPK, 16384, 16384) == 4 * 8192 * 2048 * 4
     # the 1M limit (rows past 16,384 candidates): the scores (or the survivors' keys in place)
     # [4 x 8,192 x 131,072], the segment + merge pair buffers (8 segments x 511 entries) of
     # the plain top-k, then the bound-filtered top-k's group maxima (a key per 8
