@@ -265,7 +265,7 @@ void launch_k3_regs(const K3Args& a, int64_t max_cand, int64_t grid, cudaStream_
     default: k3_topk<NT, 32, false, MODE><<<(unsigned)grid, NT, 0, st>>>(a); break;
   }
 }
-static_assert(K3_SEL_CAP == 128 * 32, "survivor selection: 128 threads x 32 keys");
+static_assert(K3_SEL_CAP == 128 * 32 && K3_SEL_CAP == kK3Threads * 8, "survivor selection: 128 x 32 or 512 x 8 keys");
 
 // One CTA per row; the block is the smallest whose registers (up to 32 keys per thread)
 // hold the launch's longest row.  Longer rows go through the segment + merge pair when
@@ -442,7 +442,12 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
         t.n_mtiles = a2.n_mtiles;
         t.row_flag = row_flag;
         t.tile_flag = tile_flag;
-        k3_topk<128, 32, false, K3_SELECT><<<(unsigned)rr, 128, 0, st>>>(t);
+        // (128 x 32 keys for the usual k; large selections, where each row keeps thousands
+        // of its survivors, spread over 512 x 8)
+        if (p.k > 1024)
+          k3_topk<kK3Threads, 8, false, K3_SELECT><<<(unsigned)rr, kK3Threads, 0, st>>>(t);
+        else
+          k3_topk<128, 32, false, K3_SELECT><<<(unsigned)rr, 128, 0, st>>>(t);
         SGQA_CUDA_OK(cudaGetLastError());
       }
       // 5. flagged rows (heavy ties) are redone from their scores: the indexer writes the
