@@ -53,11 +53,12 @@ struct K2Args {
   int32_t mode;         // K2_SCORES, K2_MAXIMA or K2_SURVIVORS
   // K2_SCORES: with tile_flag, only the (group, 128-row tile) items whose flag is set
   const int32_t* tile_flag;  // [G, n_mtiles] or null
-  // K2_MAXIMA: maxima[(g * Tc + row) * ld8 + j] = largest key of candidates 8j .. 8j+7 below
-  // the row's own block (only groups with at least one such candidate are written; 0 for
-  // a group's candidates past it); ld8 = 4 * ceil(ld / 32)
+  // K2_MAXIMA: maxima[(g * Tc + row) * ld8 + j] = largest key of candidates gs j .. gs j +
+  // gs - 1 below the row's own block, gs = 8 or 16 (only groups with at least one such
+  // candidate are written; 0 for a group's candidates past it); ld8 = 4 * ceil(ld / 32)
   uint32_t* maxima;
   int64_t ld8;
+  int32_t gs;
   // K2_SURVIVORS, row r = g * Tc + row: bit u of smask[r * ld32 + x / 32] set for candidate
   // x = 32 (x / 32) + u when its key reaches thr[r] (words of candidates below the row's own
   // block only), and that key at skeys[r * ld + x]
@@ -279,8 +280,14 @@ __global__ void __launch_bounds__(K2_THREADS, 1)
 #pragma unroll
               for (int u = 0; u < 32; ++u)
                 if (x0 + u < bt) mx[u >> 3] = max(mx[u >> 3], score_key(__uint_as_float(r[u])));
-              // groups 8j .. 8j+7 with j = x0/8 .. x0/8+3; x0 is a multiple of 32, so 16-byte aligned
-              *reinterpret_cast<uint4*>(a.maxima + rr * a.ld8 + x0 / 8) = make_uint4(mx[0], mx[1], mx[2], mx[3]);
+              if (a.gs == 16) {
+                // groups 16j .. 16j+15 with j = x0/16, x0/16+1: 8-byte aligned
+                *reinterpret_cast<uint2*>(a.maxima + rr * a.ld8 + x0 / 16) =
+                    make_uint2(max(mx[0], mx[1]), max(mx[2], mx[3]));
+              } else {
+                // groups 8j .. 8j+7 with j = x0/8 .. x0/8+3; x0 is a multiple of 32, so 16-byte aligned
+                *reinterpret_cast<uint4*>(a.maxima + rr * a.ld8 + x0 / 8) = make_uint4(mx[0], mx[1], mx[2], mx[3]);
+              }
             } else {
               uint32_t m = 0u;
               uint32_t* krow = a.skeys + rr * a.ld;

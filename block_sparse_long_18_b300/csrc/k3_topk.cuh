@@ -49,7 +49,8 @@ struct K3Args {
   int32_t nseg;         // segments per row
   int32_t prefetch_ctas;  // a CTA warms L2 for the scores of CTA blockIdx.x + prefetch_ctas (0: off)
   // bound-filtered selection (K3_THRESHOLD, K3_SELECT; row r = g * rows + i):
-  const uint32_t* keys_in;  // K3_THRESHOLD: group-maximum keys [G * rows, keys_ld], ceil(b_t / 8) per row
+  const uint32_t* keys_in;  // K3_THRESHOLD: group-maximum keys [G * rows, keys_ld], ceil(b_t / keys_gs) per row
+  int32_t keys_gs;          // K3_THRESHOLD: candidates per group (8 or 16)
   int64_t keys_ld;
   uint32_t* thr_out;        // K3_THRESHOLD: bound per row (0: none)
   const uint32_t* smask;    // K3_SELECT: survivor bits [G * rows, ld32], one per candidate below b_t
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   } else if (MODE == K3_MERGE) {
     n = pstride;
   } else if (MODE == K3_THRESHOLD) {
-    n = (bt + 7) / 8;  // groups of 8 candidates below the own block
+    n = (bt + a.keys_gs - 1) / a.keys_gs;  // groups of keys_gs candidates below the own block
     if (n <= need) {   // fewer group maxima than blocks to keep: no bound
       if (tid == 0) a.thr_out[r] = 0u;
       return;

@@ -405,18 +405,24 @@ sgqa_status run_index_topk(const Prm& p, const void* q_proxy, int64_t T, int64_t
       int32_t* row_flag = reinterpret_cast<int32_t*>(wsb + wsl.flags);  // [G * rc]
       int32_t* tile_flag = row_flag + rr;                                 // [G, n_mtiles of this pass]
       SGQA_CUDA_OK(cudaMemsetAsync(row_flag, 0, (size_t)(rr + (int64_t)p.G * a2.n_mtiles) * 4, st));
-      // 1. group maxima of the scores (nothing else leaves the SM)
+      // 1. group maxima of the scores (nothing else leaves the SM), over 16 candidates where
+      // every row still has more than k - 1 groups and keeps few of its candidates (half the
+      // bound's work; measured on B300: 1M chunk 15.2 -> 14.7 ms), else over 8 (with
+      // k = 2,048 the coarser bound's extra survivors cost more: token-level 231 -> 238 ms)
+      const int32_t gs = p.k - 1 <= 1024 && (q_start + r0) / p.B > 16 * (int64_t)(p.k - 1) ? 16 : 8;
       a2.mode = K2_MAXIMA;
       a2.maxima = maxima;
       a2.ld8 = wsl.ld8;
+      a2.gs = gs;
       SGQA_CUDA_OK(launch_k2(a2, ta, tb, tc, st));
       // 2. each row's bound: the (k-1)-th largest of its group maxima
       {
         K3Args t = a3;
         t.keys_in = maxima;
         t.keys_ld = wsl.ld8;
+        t.keys_gs = gs;
         t.thr_out = thr;
-        const int64_t n_max = cdiv(cand_last, 8), grid = rr;
+        const int64_t n_max = cdiv(cand_last, gs), grid = rr;
         if (n_max <= 128 * kK3Per)
           launch_k3_regs<128, K3_THRESHOLD>(t, n_max, grid, st);
         else if (n_max <= 256 * kK3Per)
