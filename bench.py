@@ -578,9 +578,19 @@ def run_sgqa(args, rank, world, local_rank):
     # one; the grouped mode two more for the row order)
     kind = sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start)
     launches_per_step = 2 + {sgqa.ATTN_ROUTED: 3, sgqa.ATTN_GROUPED: 5}.get(kind, 0)
+    # per indexer + top-k pass: the indexer and one top-k launch (two for rows past 16,384
+    # candidates: slices and merge); a bound-filtered pass (the default workspace holds its
+    # buffers) six: indexer maxima, bounds, indexer survivors, selection, and the two
+    # launches for rows with too many survivors (they return at once when none has)
+    need = wl.k - 1
+    max_cand = (wl.q_start + wl.T - 1) // wl.B
+    filtered_fits = wl.k >= 2 and need <= 4096 and 8 * need < max_cand <= 8 * 16384
     for r0 in range(0, wl.T, 8192):
         cand_last = (wl.q_start + min(wl.T, r0 + 8192) - 1) // wl.B
-        launches_per_step += (1 if cand_last > 0 else 0) + (2 if cand_last > 16384 and wl.k > 1 else 1)
+        if filtered_fits and (wl.q_start + r0) // wl.B > max(8 * need, FILTERED_MIN_CAND):
+            launches_per_step += 6
+        else:
+            launches_per_step += (1 if cand_last > 0 else 0) + (2 if cand_last > 16384 and wl.k > 1 else 1)
     clocks = clk.summary()
     out = {
         "metric": METRIC,
