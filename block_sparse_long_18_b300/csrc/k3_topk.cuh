@@ -74,6 +74,7 @@ enum K3Mode : int {
                      // place); writes the final selection
 };
 constexpr int K3_SEL_CAP = 4096;  // survivors a K3_SELECT row may hold (128 threads x 32)
+constexpr int K3_SEL_MAX_WORDS = 131072 / 32;  // mask words of the longest K3_SELECT row
 
 
 // Inclusive warp scan.
@@ -202,15 +203,20 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
   const uint32_t* mkeys = MODE == K3_THRESHOLD ? a.keys_in + r * a.keys_ld : a.pair_key + r * pstride;
   if (MODE == K3_SELECT) {
     // The survivors' candidate indices, in index order, from the mask words: thread tid
-    // scans words [tid W, tid W + W), one block scan places its survivors.
+    // takes words [tid WPT, tid WPT + WPT), all loaded before the first is used (their
+    // latencies overlap), and one block scan places its survivors.
+    constexpr int WPT = (K3_SEL_MAX_WORDS + NT - 1) / NT;
     const uint32_t* mrow = a.smask + r * a.ld32;
-    const int64_t n_words = (bt + 31) / 32;
-    const int64_t W = (n_words + NT - 1) / NT;
-    uint32_t c = 0;
-    for (int64_t w = 0; w < W; ++w) {
-      const int64_t wi = (int64_t)tid * W + w;
-      if (wi < n_words) c += (uint32_t)__popc(__ldg(mrow + wi));
+    const int64_t n_words = (bt + 31) / 32;  // <= K3_SEL_MAX_WORDS: rows of at most 131,072 candidates
+    uint32_t words[MODE == K3_SELECT ? WPT : 1];
+#pragma unroll
+    for (int w = 0; w < WPT; ++w) {
+      const int64_t wi = (int64_t)tid * WPT + w;
+      words[MODE == K3_SELECT ? w : 0] = wi < n_words ? __ldg(mrow + wi) : 0u;
     }
+    uint32_t c = 0;
+#pragma unroll
+    for (int w = 0; w < WPT; ++w) c += (uint32_t)__popc(words[MODE == K3_SELECT ? w : 0]);
     uint32_t total;
     uint32_t o = k3_block_excl_scan<NT>(c, warp_tot, total);
     if (total > (uint32_t)a.cap) {  // more survivors than one CTA holds: redone from the scores
@@ -220,9 +226,10 @@ __global__ void __launch_bounds__(NT, STREAM ? 1 : 1024 / NT) k3_topk(const __gr
       }
       return;
     }
-    for (int64_t w = 0; w < W; ++w) {
-      const int64_t wi = (int64_t)tid * W + w;
-      uint32_t bits = wi < n_words ? __ldg(mrow + wi) : 0u;
+#pragma unroll
+    for (int w = 0; w < WPT; ++w) {
+      const int64_t wi = (int64_t)tid * WPT + w;
+      uint32_t bits = words[MODE == K3_SELECT ? w : 0];
       while (bits != 0u) {
         const uint32_t b = (uint32_t)__ffs(bits) - 1u;
         bits &= bits - 1u;
