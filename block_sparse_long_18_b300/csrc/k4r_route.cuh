@@ -77,10 +77,19 @@ __global__ void __launch_bounds__(K4R_WARPS * 32) k4r_count(const K4RouteArgs a)
       const int32_t cnt = __shfl_sync(0xffffffffu, cnt_l, r), bt = __shfl_sync(0xffffffffu, bt_l, r);
       const int64_t row = __shfl_sync(0xffffffffu, row_l, r);
       const int32_t* sel = a.sel_idx + ((int64_t)g * a.rows + row) * a.kcap;
-      for (int32_t j = (int32_t)lane; j < cnt; j += 32) {
-        const int32_t b = __ldg(sel + j);
-        const int32_t o = b - wb;
-        if (b >= 0 && b <= bt && o >= 0 && o < K4U_WIN) atomicOr(&bm[o >> 5], 1u << (o & 31));
+      // 512 entries at a time, every load issued before the first is used
+      for (int32_t j0 = 0; j0 < cnt; j0 += 512) {
+        int32_t e[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int32_t j = j0 + (int32_t)lane + 32 * q;
+          e[q] = j < cnt ? __ldg(sel + j) : -1;
+        }
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const int32_t b = e[q], o = b - wb;
+          if (b >= 0 && b <= bt && o >= 0 && o < K4U_WIN) atomicOr(&bm[o >> 5], 1u << (o & 31));
+        }
       }
     }
     __syncwarp();
@@ -193,11 +202,21 @@ __global__ void __launch_bounds__(K4G_SIG_WARPS * 32) k4g_signature(const K4Grou
   if (c < 1 || c > cap) c = c < 1 ? 1 : cap;
   const int32_t* sel = a.sel_idx + r * a.kcap;
   uint32_t h1 = ~0u, h2 = ~0u;
-  for (int32_t j = (int32_t)lane; j < c; j += 32) {
-    const int32_t b = __ldg(sel + j);
-    if (b < 0 || b > bt) continue;
-    h1 = min(h1, k4g_mix((uint32_t)b));
-    h2 = min(h2, k4g_mix((uint32_t)b ^ K4G_SEED2));
+  // 512 entries at a time, every load issued before the first is used
+  for (int32_t j0 = 0; j0 < c; j0 += 512) {
+    int32_t e[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int32_t j = j0 + (int32_t)lane + 32 * q;
+      e[q] = j < c ? __ldg(sel + j) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int32_t b = e[q];
+      if (b < 0 || b > bt) continue;
+      h1 = min(h1, k4g_mix((uint32_t)b));
+      h2 = min(h2, k4g_mix((uint32_t)b ^ K4G_SEED2));
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
