@@ -8,13 +8,14 @@
 // Layout: k_proxy [G, ctx_cap, P] bf16 -> k_blk [G, nb_cap, P] bf16.  Each thread owns 8
 // consecutive proxy elements (one 16-byte vector) of one block, so a warp reads whole
 // 512-byte token rows (P = 256) and writes a whole 512-byte block row.  The sum runs in
-// fp32 in token order; full blocks multiply by 1/B (exact, B is a power of two), partial
-// blocks divide in double so that the result is rounded to bf16 only once.
+// fp32 in token order; full blocks multiply by 1/B (exact, B is a power of two), and a
+// partial block of n tokens rounds sum / n to bf16 as if the quotient were exact
+// (k1_partial_mean).
 //
 // The decode cache can hold the block index as FP8 E4M3 instead (the pages deploy the model
 // in FP8; this cache is a variant): the same fp32 sum, rounded once to E4M3 (to nearest,
-// ties to even, saturating at +-448) by the hardware conversion -- from fp32 for full
-// blocks (x 1/B is exact) and from fp64 for partial ones.
+// ties to even, saturating at +-448) by the hardware conversion from the same fp32 value
+// (x 1/B for full blocks, k1_partial_mean for partial ones).
 #pragma once
 #include <cuda_fp8.h>
 #include "ptx.cuh"
@@ -33,11 +34,26 @@ struct K1Args {
   const int64_t* seq_tok_end;  // device or nullptr
 };
 
+// A partial block of n < B <= 16 tokens rounds sum / n once.  In place of a double division
+// (B300's FP64 unit is slow: the partial blocks of one decode step took about 10 us), the
+// fp32 quotient q = RN32(s / n) is rounded to bf16 or E4M3, which gives the same result:
+// - a rounding midpoint m of either format has at most 9 significant bits, so s - n m is a
+//   multiple of 2^min(e_s, e_m), e_s the last bit of s and e_m that of m; if s / n != m it
+//   misses m by at least 2^e_s / n (or 2^e_m / n, larger still);
+// - 2^e_s > |s| 2^-24 = n |s / n| 2^-24, and for n not a power of two the power of two
+//   2^e_s exceeds n |m| 2^-24 by enough that s / n misses m by more than half of m's fp32
+//   step, so q = m only when s / n = m (n a power of two divides exactly);
+// - no midpoint lies strictly between s / n and q, q being the fp32 value nearest s / n.
+// The argument holds while s / n is a normal fp32 number: sums of magnitude below 2^-100
+// (other than zero) still divide in double.
+__device__ __forceinline__ bool k1_partial_fp32_ok(float acc) { return acc == 0.f || fabsf(acc) >= 0x1p-100f; }
+
 // The 8 means of one thread, stored as bf16 (16 bytes) or E4M3 (8 bytes) at element `e0`
 // of the block row.
 template <bool E4M3>
 __device__ __forceinline__ void k1_store(void* row, int pv, const float (&acc)[8], int64_t n, int B) {
   const float inv_b = 1.0f / (float)B;
+  const float fn = (float)n;
   if (!E4M3) {
     uint4 o;
     uint32_t* op = reinterpret_cast<uint32_t*>(&o);
@@ -45,13 +61,14 @@ __device__ __forceinline__ void k1_store(void* row, int pv, const float (&acc)[8
 #pragma unroll
       for (int e = 0; e < 4; ++e) op[e] = pack_bf16(acc[2 * e] * inv_b, acc[2 * e + 1] * inv_b);
     } else {
-      const double dn = (double)n;
+      __nv_bfloat16 h[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __nv_bfloat16 lo = __double2bfloat16((double)acc[2 * e] / dn);
-        __nv_bfloat16 hi = __double2bfloat16((double)acc[2 * e + 1] / dn);
-        op[e] = (uint32_t)__bfloat16_as_ushort(lo) | ((uint32_t)__bfloat16_as_ushort(hi) << 16);
-      }
+      for (int e = 0; e < 8; ++e)
+        h[e] = k1_partial_fp32_ok(acc[e]) ? __float2bfloat16_rn(__fdiv_rn(acc[e], fn))
+                                          : __double2bfloat16((double)acc[e] / (double)n);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        op[e] = (uint32_t)__bfloat16_as_ushort(h[2 * e]) | ((uint32_t)__bfloat16_as_ushort(h[2 * e + 1]) << 16);
     }
     reinterpret_cast<uint4*>(row)[pv] = o;
   } else {
@@ -60,9 +77,11 @@ __device__ __forceinline__ void k1_store(void* row, int pv, const float (&acc)[8
 #pragma unroll
       for (int e = 0; e < 8; ++e) c[e] = __nv_cvt_float_to_fp8(acc[e] * inv_b, __NV_SATFINITE, __NV_E4M3);
     } else {
-      const double dn = (double)n;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) c[e] = __nv_cvt_double_to_fp8((double)acc[e] / dn, __NV_SATFINITE, __NV_E4M3);
+      for (int e = 0; e < 8; ++e)
+        c[e] = k1_partial_fp32_ok(acc[e])
+                   ? __nv_cvt_float_to_fp8(__fdiv_rn(acc[e], fn), __NV_SATFINITE, __NV_E4M3)
+                   : __nv_cvt_double_to_fp8((double)acc[e] / (double)n, __NV_SATFINITE, __NV_E4M3);
     }
     uint2 o;
     o.x = (uint32_t)c[0] | ((uint32_t)c[1] << 8) | ((uint32_t)c[2] << 16) | ((uint32_t)c[3] << 24);

@@ -1130,8 +1130,10 @@ static sgqa_status run_decode(const sgqa_params* prm, int32_t batch, const int64
       a2.kv_off[i] = kv_off[i];
     }
     dim3 grid((unsigned)cdiv(max_cand, a2.rows_per_cta), (unsigned)(p.G * batch));
-    if (e4m3)
-      k2d_decode_index_e4m3<<<grid, 256, 0, st>>>(a2);
+    if (e4m3 && p.P == 192)
+      k2d_decode_index_e4m3<true><<<grid, 256, 0, st>>>(a2);
+    else if (e4m3)
+      k2d_decode_index_e4m3<false><<<grid, 256, 0, st>>>(a2);
     else
       k2d_decode_index<<<grid, 256, 0, st>>>(a2);
     SGQA_CUDA_OK(cudaGetLastError());

@@ -68,10 +68,12 @@ def _check_sequences(inp, wl, res, seqs, gate_per_dim=1):
             assert np.max(np.abs(lse[s, hs].cpu().numpy() - ref_lse[0])) <= LSE_ABS
 
 
-def test_decode_ragged_small(sg):
-    wl = gen.Workload("dec_small", T=1, C=0, G=2, Hg=16, k=16, batch=5, ctx_lo=1, ctx_hi=3000)
+@pytest.mark.parametrize("P", [256, 192])
+def test_decode_ragged_small(sg, P):
+    """Ragged contexts (1 .. 3,000 tokens); P = 192 leaves 8 lanes of the indexer's row load idle."""
+    wl = gen.Workload(f"dec_small_P{P}", T=1, C=0, G=2, Hg=16, P=P, k=16, batch=5, ctx_lo=1, ctx_hi=3000)
     inp = gen.make_decode_inputs(wl, seed=4, device="cuda")
-    prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k)
+    prm = sg.params(G=wl.G, Hg=wl.Hg, P=P, k=wl.k)
     res = _run_decode(sg, inp, wl, prm)
     _check_sequences(inp, wl, res, range(wl.batch))
 

@@ -87,10 +87,11 @@ def _check_sequences_fp8(inp, wl, res, seqs):
             assert np.max(np.abs(lse[s, hs].cpu().numpy() - ref_lse[0])) <= LSE_ABS
 
 
-@pytest.mark.parametrize("P", [256, 128, 64])
+@pytest.mark.parametrize("P", [256, 192, 128, 64])
 def test_decode_fp8_ragged(sg, P):
     """Ragged contexts (1 .. 3,000 tokens, partial newest blocks) for every proxy width the
-    E4M3 indexer lays out differently (16, 8 or 4 lanes per cache row)."""
+    E4M3 indexer lays out differently (16, 8 or 4 lanes per cache row; P = 192 takes 16
+    lanes of which 12 hold codes)."""
     wl = gen.Workload(f"dec8_P{P}", T=1, C=0, G=2, Hg=16, P=P, k=16, batch=5, ctx_lo=1, ctx_hi=3000)
     inp = gen.make_decode_inputs(wl, seed=32, device="cuda")
     prm = sg.params(G=wl.G, Hg=wl.Hg, P=P, k=wl.k)

@@ -99,6 +99,7 @@ SMALL = [
     dict(T=150, G=1, Hg=4, B=2, k=20),                    # B = 2
     dict(T=260, G=1, Hg=1, B=8, k=7, P=64),               # P = 64, single head
     dict(T=333, G=2, Hg=16, B=8, k=40, P=128, planted=True),
+    dict(T=300, G=2, Hg=8, B=8, k=12, P=192),             # P = 192: three 64-wide indexer chunks
 ]
 
 
