@@ -95,8 +95,9 @@ enum { SGQA_OP_INDEX_TOPK = 1, SGQA_OP_PREFILL = 2, SGQA_OP_DECODE = 3, SGQA_OP_
  * historical positions into block representations with block size 8").
  *
  * k_blk[g, b, :] = bf16( mean of k_proxy[g, j, :] over the tokens j of block b that lie
- * before tok_end ), accumulated in fp32 in token order and rounded once to nearest-even,
- * for every block b that holds a token of [tok_begin, tok_end).  A block that is only
+ * before tok_end ), accumulated in fp32 in token order and rounded once to nearest-even
+ * (the fp32 sum divided by the token count rounds as the exact quotient would), for every
+ * block b that holds a token of [tok_begin, tok_end).  A block that is only
  * partly filled averages the tokens present; it is rebuilt when more tokens arrive.
  *
  *   k_proxy  [G, ctx_cap, P] bf16, read
@@ -308,9 +309,9 @@ SGQA_API sgqa_status sgqa_index_topk_noalloc(const sgqa_params* prm, const void*
  * bytes the decode indexer streams.
  *
  * sgqa_build_block_index_fp8: as sgqa_build_block_index, but k_blk_e4m3 is uint8 codes
- *   [G, nb_cap, P]; each block mean (fp32 sum of the bf16 proxies, times 1/B, or divided
- *   in fp64 for a partial block) is rounded once to E4M3, to nearest, ties to even,
- *   saturating at +-448.  Base 16-byte aligned.
+ *   [G, nb_cap, P]; each block mean (fp32 sum of the bf16 proxies over the tokens
+ *   present, divided by their number) is rounded once to E4M3 as the exact quotient would
+ *   be, to nearest, ties to even, saturating at +-448.  Base 16-byte aligned.
  * sgqa_decode_fp8: as sgqa_decode, but k_blk_cache_e4m3 is uint8 codes [G, total / B, P]
  *   (the rebuilt block is written as E4M3).  Scores widen the codes exactly to fp32.
  * ------------------------------------------------------------------------------- */
