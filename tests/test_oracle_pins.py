@@ -87,6 +87,27 @@ def _rne_fraction_bf16(fr: Fraction) -> float:
     return sign * float(fl * q)
 
 
+def _rne_fraction_e4m3(fr: Fraction) -> float:
+    """Independent exact rounding of a rational to FP8 E4M3: 4 significant bits, a fixed
+    step of 2^-9 below 2^-6 (subnormals), ties to even, magnitude saturating at 448."""
+    if fr == 0:
+        return 0.0
+    sign = -1 if fr < 0 else 1
+    a = abs(fr)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    q = Fraction(2) ** (max(e, -6) - 3)
+    n = a / q
+    fl = n.numerator // n.denominator
+    rem = n - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * min(float(fl * q), 448.0)
+
+
 # ---------------------------------------------------------------------------------------
 # FP8 E4M3 (the decode block-proxy cache variant)
 # ---------------------------------------------------------------------------------------
@@ -202,6 +223,36 @@ def test_block_index_general_values_match_exact_rational_mean():
         for p in range(P):
             s = sum(Fraction(float(x)) for x in vals[0, b * B:(b + 1) * B, p])
             assert oracle.bf16_to_f64(kb[0, b, p:p + 1])[0] == _rne_fraction_bf16(s / B)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "e4m3"])
+def test_partial_block_means_at_rounding_midpoints(fmt):
+    """Partial blocks (n = 3, 5, 6, 7 tokens) whose exact sums sit on n times a rounding
+    midpoint of bf16 or E4M3, or up to three fp32 steps beside it: the oracle's mean equals
+    the exact rational mean rounded once (ties to even only on the midpoints themselves)."""
+    from midpoint_sums import midpoint_sums, split_bf16
+
+    rng = np.random.default_rng(41 if fmt == "bf16" else 42)
+    G, P, B, nblk = 1, 16, 8, 48
+    n = np.array([(3, 5, 6, 7)[i % 4] for i in range(nblk)])
+    s = midpoint_sums(rng, np.broadcast_to(n[None, :, None], (G, nblk, P)).astype(np.float64), fmt, max_steps=3)
+    t0, t1, t2 = split_bf16(s)
+    kp = np.zeros((G, nblk, B, P), np.float32)
+    kp[:, :, 0], kp[:, :, 1], kp[:, :, 2] = t0, t1, t2
+    kp = _bits(torch.from_numpy(kp.reshape(G, nblk * B, P)).to(torch.bfloat16))
+    build = oracle.block_index_e4m3 if fmt == "e4m3" else oracle.block_index
+    kb = np.zeros((G, nblk, P), np.uint8 if fmt == "e4m3" else np.uint16)
+    for i in range(nblk):
+        kb = build(kp, B, i * B, i * B + int(n[i]), k_blk=kb, nb_cap=nblk)
+    got = oracle.e4m3_to_f64(kb) if fmt == "e4m3" else oracle.bf16_to_f64(kb)
+    rne = _rne_fraction_e4m3 if fmt == "e4m3" else _rne_fraction_bf16
+    ties = 0
+    for i in range(nblk):
+        for p in range(P):
+            exact = Fraction(float(s[0, i, p])) / int(n[i])
+            assert got[0, i, p] == rne(exact), (i, p)
+            ties += rne(exact) != rne(exact * (1 + Fraction(1, 1 << 40)))
+    assert ties > 0  # some sums are exact midpoints: the tie rule is exercised
 
 
 # ---------------------------------------------------------------------------------------
