@@ -99,6 +99,20 @@ def test_decode_fp8_ragged(sg, P):
     _check_sequences_fp8(inp, wl, res, range(wl.batch))
 
 
+@pytest.mark.parametrize("scale", [2.0 ** 17, 2.0 ** -30], ids=["q_above_f16_range", "q_below_f16_range"])
+def test_decode_fp8_query_not_f16_exact(sg, scale):
+    """Query proxies scaled by a power of two out of f16's exact range (past 65,504, or below
+    its smallest subnormal): the indexer's products then come from fp32 operands rather than
+    f16 ones; selections and outputs still equal the oracle's."""
+    wl = gen.Workload("dec8_qscale", T=1, C=0, G=2, Hg=16, k=16, batch=4, ctx_lo=1, ctx_hi=3000)
+    inp = gen.make_decode_inputs(wl, seed=33, device="cuda")
+    inp.q_proxy = (inp.q_proxy.float() * scale).to(torch.bfloat16)
+    assert not torch.equal(inp.q_proxy.float(), inp.q_proxy.half().float())
+    prm = sg.params(G=wl.G, Hg=wl.Hg, k=wl.k)
+    res = _run_decode_fp8(sg, inp, wl, prm)
+    _check_sequences_fp8(inp, wl, res, range(wl.batch))
+
+
 def test_decode_fp8_full_config_sampled_sequences(sg):
     """The 8-sequence decode workload (contexts uniform in [256K, 1M]) over an E4M3 cache;
     the shortest and the longest sequence are checked in full."""
