@@ -69,8 +69,8 @@ def work_model(wl):
     w["k2_bytes"] = G * P * 2 * (T + (q0 + T) // B) + 4 * G * sum_bt
     w["k3_bytes"] = 4 * G * sum_bt + 4 * G * sum_n
     w["k4_flop"] = 4 * D * H * sum_att
-    # per-(row, group) gathers: every kept block read once per row that keeps it (the
-    # survey's primary K4 line; a kernel that shares gathers across rows moves far less)
+    # per-(row, group) gathers: every kept block read once per row that keeps it (a line
+    # for a kernel that gathers per row; one that shares gathers across rows moves far less)
     w["k4_gather_bytes"] = 2 * 2 * D * B * G * sum_n
     # bytes every K4 must move: Q, gate and O once, the selection and LSE once, and K/V of
     # every block some row selected once (set by the caller from the selection, else every
@@ -445,8 +445,8 @@ def run_sgqa(args, rank, world, local_rank):
     ms = max_over_ranks(float(step_ms.mean()), world, dev)
     value = job_value(wl.T, world, ms)
 
-    # ---- roofline of each stage (survey's per-stage line: max of FLOPs at the bf16 peak and
-    # algorithmic bytes at the HBM peak, both measured on the B300s) ----
+    # ---- roofline of each stage (max of its FLOPs at the bf16 peak and its algorithmic
+    # bytes at the HBM peak, both peaks measured on B300) ----
     w = work_model(wl)
     attn_kind = sgqa.sgqa_attention_kernel(prm, wl.T, wl.q_start)
     sel_stats = selection_stats(plan, wl, grouped=attn_kind == sgqa.ATTN_GROUPED)

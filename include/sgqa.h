@@ -54,7 +54,7 @@ typedef struct CUstream_st* sgqa_stream_t;
 typedef enum {
   SGQA_OK = 0,
   SGQA_ERR_INVALID_ARGUMENT = 1,   /* null pointer, negative size, inconsistent ranges */
-  SGQA_ERR_UNSUPPORTED_SHAPE = 2,  /* a dimension this build does not implement */
+  SGQA_ERR_UNSUPPORTED_SHAPE = 2,  /* a dimension the library does not implement */
   SGQA_ERR_WORKSPACE_TOO_SMALL = 3,/* ws_bytes below sgqa_workspace_bytes() */
   SGQA_ERR_CUDA = 4,               /* a CUDA runtime call failed (launch, attribute, ...) */
   SGQA_ERR_DEVICE_TIMEOUT = 5,     /* a device-side bounded wait ran out */
@@ -64,7 +64,7 @@ typedef enum {
 typedef struct {
   int32_t num_kv_groups;    /* G >= 1 (4 on the pages) */
   int32_t heads_per_group;  /* Hg in 1..16 (16 on the pages; the 16 heads are the MMA M dim) */
-  int32_t head_dim;         /* D; this build implements 192 */
+  int32_t head_dim;         /* D; the library implements 192 */
   int32_t proxy_dim;        /* P in {64, 128, 192, 256} (256 on the pages) */
   int32_t block_size;       /* B in {1, 2, 4, 8, 16} (8 on the pages; 1 = token-level reference) */
   int32_t top_k_blocks;     /* k >= 1 (512 on the pages = 4,096 tokens) */
