@@ -78,11 +78,11 @@ def test_decode_ragged_small(sg, P):
     _check_sequences(inp, wl, res, range(wl.batch))
 
 
-@pytest.mark.parametrize("B,k,gate_per_dim", [(16, 8, 1), (4, 12, 1), (8, 10, 0)],
-                         ids=["B16", "B4_cp_async", "per_head_gate"])
+@pytest.mark.parametrize("B,k,gate_per_dim", [(16, 8, 1), (4, 12, 1), (2, 24, 1), (1, 48, 1), (8, 10, 0)],
+                         ids=["B16", "B4_bulk_copy", "B2_bulk_copy", "B1_token_level", "per_head_gate"])
 def test_decode_ragged_block_sizes_and_gates(sg, B, k, gate_per_dim):
-    """Ragged contexts with blocks of 16 (one block per stage), blocks of 4 (the cp.async
-    loader with split-K), and a per-head gate."""
+    """Ragged contexts with blocks of 16 (one block per stage), blocks of 4, 2 and 1 (the
+    bulk-copy loader with split-K; B = 1 is token-level selection), and a per-head gate."""
     wl = gen.Workload(f"dec_B{B}", T=1, C=0, G=2, Hg=16, B=B, k=k, batch=4, ctx_lo=1, ctx_hi=2500)
     inp = gen.make_decode_inputs(wl, seed=6, device="cuda")
     if not gate_per_dim:
