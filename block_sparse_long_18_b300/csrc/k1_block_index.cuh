@@ -10,12 +10,12 @@
 // 512-byte token rows (P = 256) and writes a whole 512-byte block row.  The sum runs in
 // fp32 in token order; full blocks multiply by 1/B (exact, B is a power of two), and a
 // partial block of n tokens rounds sum / n to bf16 as if the quotient were exact
-// (k1_partial_mean).
+// (k1_partial_fp32_ok).
 //
 // The decode cache can hold the block index as FP8 E4M3 instead (the pages deploy the model
 // in FP8; this cache is a variant): the same fp32 sum, rounded once to E4M3 (to nearest,
 // ties to even, saturating at +-448) by the hardware conversion from the same fp32 value
-// (x 1/B for full blocks, k1_partial_mean for partial ones).
+// (x 1/B for full blocks, the fp32 quotient of k1_partial_fp32_ok for partial ones).
 #pragma once
 #include <cuda_fp8.h>
 #include "ptx.cuh"
