@@ -38,6 +38,22 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib._lib, name)
 
 
+def test_header_is_plain_c(tmp_path):
+    """The header needs no CUDA, torch or C++ headers: it compiles as strict C99 and as C++11,
+    and a C program can take the address of every declared entry point."""
+    names = _declared()
+    src = tmp_path / "use.c"
+    src.write_text('#include "sgqa.h"\nint main(void) {\n  void* p[] = {' +
+                   ", ".join(f"(void*){n}" for n in names) + "};\n  return p[0] == 0;\n}\n")
+    inc = os.path.join(ROOT, "include")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", inc, "-fsyntax-only", str(src)],
+                   check=True, capture_output=True)
+    cpp = tmp_path / "use.cpp"
+    cpp.write_text('#include "sgqa.h"\nint main() { return 0; }\n')
+    subprocess.run(["g++", "-std=c++11", "-Wall", "-Wextra", "-Werror", "-I", inc, "-fsyntax-only", str(cpp)],
+                   check=True, capture_output=True)
+
+
 def test_abi_version(lib):
     assert lib.abi_version() == 2
 
